@@ -1,0 +1,301 @@
+"""Pins for the fp64 oracle (CPU only).
+
+The oracle is checked against things that do not come from the oracle:
+an independent pure-Python brute force, closed forms, invariants that the
+mathematics of softmax attention fixes, exact decoders checked against
+library conversions, and library routines for the special cases that reduce
+to them.  Each test is chosen so that a plausible slip in the oracle (a
+dropped scale, a wrong sign, a swapped B/S/H index, a wrong causal offset,
+a V/K mix-up, a base-2 LSE) fails at least one of them.
+"""
+import itertools
+import math
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+
+
+# --------------------------------------------------------------------------
+# an independent brute force: plain Python floats, explicit visible sets
+# --------------------------------------------------------------------------
+def brute_force(q, k, v, scale, causal):
+    """q [B,Sq,H,D], k/v [B,Sk,H,D] nested lists -> O [B,Sq,H,Dv], LSE [B,H,Sq]."""
+    B, Sq, H = len(q), len(q[0]), len(q[0][0])
+    Sk = len(k[0])
+    Dv = len(v[0][0][0]) if Sk else 0
+    O = [[[None] * H for _ in range(Sq)] for _ in range(B)]
+    L = [[[None] * Sq for _ in range(H)] for _ in range(B)]
+    for b in range(B):
+        for h in range(H):
+            for i in range(Sq):
+                vis = [j for j in range(Sk) if (not causal) or (j - i <= Sk - Sq)]
+                if not vis:
+                    O[b][i][h] = [0.0] * len(v[0][0][0]) if Sk else [0.0]
+                    L[b][h][i] = -math.inf
+                    continue
+                s = {j: scale * sum(a * c for a, c in zip(q[b][i][h], k[b][j][h])) for j in vis}
+                e = {j: math.exp(s[j]) for j in vis}  # tiny values: no overflow
+                z = sum(e.values())
+                O[b][i][h] = [sum(e[j] * v[b][j][h][c] for j in vis) / z for c in range(Dv)]
+                L[b][h][i] = math.log(z)
+    return O, L
+
+
+def _rand(shape, rng):
+    return np.asarray(rng.standard_normal(shape), dtype=np.float64)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_brute_force_tiny(seed):
+    rng = np.random.default_rng(seed)
+    B, H = rng.integers(1, 3), rng.integers(1, 4)
+    Sq, Sk = int(rng.integers(1, 9)), int(rng.integers(1, 9))
+    D, Dv = int(rng.integers(1, 5)), int(rng.integers(1, 5))
+    causal = bool(seed % 2)
+    scale = float(rng.uniform(0.2, 1.5))
+    q, k, v = _rand((B, Sq, H, D), rng), _rand((B, Sk, H, D), rng), _rand((B, Sk, H, Dv), rng)
+    o, lse = oracle.attention(q, k, v, softmax_scale=scale, causal=causal)
+    O, L = brute_force(q.tolist(), k.tolist(), v.tolist(), scale, causal)
+    O = np.array(O, dtype=np.float64)
+    L = np.array(L, dtype=np.float64)
+    fin = np.isfinite(L)
+    assert np.array_equal(fin, np.isfinite(lse))
+    assert np.allclose(lse[fin], L[fin], rtol=0, atol=1e-12)
+    assert np.all(lse[~fin] == -np.inf)
+    assert np.allclose(o, O, rtol=0, atol=1e-12)
+
+
+def test_hand_worked_two_keys():
+    # one query q = (1, 0), keys (1,0) and (0,1), scale 1: s = (1, 0)
+    # softmax = (e/(e+1), 1/(e+1)); O = softmax . V ; LSE = ln(e + 1)
+    q = np.array([[[[1.0, 0.0]]]])
+    k = np.array([[[[1.0, 0.0]], [[0.0, 1.0]]]])
+    v = np.array([[[[1.0, 2.0]], [[3.0, 4.0]]]])
+    o, lse = oracle.attention(q, k, v, softmax_scale=1.0)
+    e = math.e
+    p0, p1 = e / (e + 1), 1 / (e + 1)
+    assert o[0, 0, 0] == pytest.approx([p0 * 1 + p1 * 3, p0 * 2 + p1 * 4], abs=1e-15)
+    assert lse[0, 0, 0] == pytest.approx(math.log(e + 1), abs=1e-15)
+    # scale 2 and causal (row 0 sees key 0 only when Sq == Sk == 1 ... here Sq=1,Sk=2:
+    # bottom-right alignment lets row 0 see keys j <= 0 + 2 - 1 = 1, i.e. both)
+    o2, lse2 = oracle.attention(q, k, v, softmax_scale=2.0, causal=True)
+    e2 = math.exp(2.0)
+    assert lse2[0, 0, 0] == pytest.approx(math.log(e2 + 1), abs=1e-15)
+    assert o2[0, 0, 0, 0] == pytest.approx((e2 * 1 + 3) / (e2 + 1), abs=1e-15)
+
+
+def test_constant_v_returns_that_row():
+    rng = np.random.default_rng(1)
+    q, k = _rand((2, 7, 3, 5), rng), _rand((2, 9, 3, 5), rng)
+    c = rng.standard_normal(4)
+    v = np.broadcast_to(c, (2, 9, 3, 4)).copy()
+    for causal in (False, True):
+        o, _ = oracle.attention(q, k, v, softmax_scale=0.7, causal=causal)
+        assert np.allclose(o, np.broadcast_to(c, o.shape), atol=1e-13)
+
+
+@pytest.mark.parametrize("causal,sq,sk", [(False, 6, 10), (True, 10, 10), (True, 4, 9),
+                                          (True, 9, 4)])
+def test_zero_q_gives_log_count_and_mean(causal, sq, sk):
+    rng = np.random.default_rng(2)
+    q = np.zeros((1, sq, 2, 8))
+    k, v = _rand((1, sk, 2, 8), rng), _rand((1, sk, 2, 3), rng)
+    o, lse = oracle.attention(q, k, v, softmax_scale=0.35, causal=causal)
+    for i in range(sq):
+        n = sk if not causal else max(0, min(sk, i + sk - sq + 1))
+        for h in range(2):
+            if n == 0:
+                assert lse[0, h, i] == -np.inf and np.all(o[0, i, h] == 0)
+            else:
+                assert lse[0, h, i] == pytest.approx(math.log(n), abs=1e-13)
+                assert np.allclose(o[0, i, h], v[0, :n, h].mean(axis=0), atol=1e-13)
+
+
+def test_causal_row_zero_is_v0():
+    rng = np.random.default_rng(3)
+    q, k, v = _rand((2, 12, 2, 6), rng), _rand((2, 12, 2, 6), rng), _rand((2, 12, 2, 6), rng)
+    o, lse = oracle.attention(q, k, v, softmax_scale=0.41, causal=True)
+    assert np.allclose(o[:, 0], v[:, 0], atol=1e-14)
+    s00 = 0.41 * np.einsum("bhd,bhd->bh", q[:, 0], k[:, 0])
+    assert np.allclose(lse[:, :, 0], s00, atol=1e-14)
+
+
+def test_empty_keys_give_zero_and_minus_inf():
+    rng = np.random.default_rng(4)
+    q = _rand((1, 5, 2, 4), rng)
+    k = np.zeros((1, 0, 2, 4))
+    v = np.zeros((1, 0, 2, 4))
+    o, lse = oracle.attention(q, k, v, softmax_scale=1.0)
+    assert np.all(o == 0) and np.all(lse == -np.inf)
+
+
+def test_probabilities_sum_to_one_and_masked_are_zero():
+    rng = np.random.default_rng(5)
+    B, Sq, Sk, H = 1, 6, 8, 2
+    q, k, v = _rand((B, Sq, H, 4), rng), _rand((B, Sk, H, 4), rng), _rand((B, Sk, H, 4), rng)
+    rows = oracle.all_rows(B, H, seqlen_q=Sq)
+    o, lse, p = oracle.attention_rows(q, k, v, rows, softmax_scale=0.5, causal=True,
+                                      return_probs=True)
+    assert np.allclose(p.sum(axis=1), 1.0, atol=1e-14)
+    for r, (_, _, i) in enumerate(rows):
+        last = i + Sk - Sq
+        assert np.all(p[r, last + 1:] == 0) and np.all(p[r, :last + 1] > 0)
+    # O is the probability-weighted sum of V rows
+    for r, (b, h, i) in enumerate(rows):
+        assert np.allclose(o[r], p[r] @ v[b, :, h], atol=1e-14)
+
+
+def test_permutation_invariance_noncausal():
+    rng = np.random.default_rng(6)
+    q, k, v = _rand((2, 5, 3, 4), rng), _rand((2, 11, 3, 4), rng), _rand((2, 11, 3, 6), rng)
+    o, lse = oracle.attention(q, k, v, softmax_scale=0.8)
+    perm = rng.permutation(11)
+    o2, lse2 = oracle.attention(q, k[:, perm], v[:, perm], softmax_scale=0.8)
+    assert np.allclose(o, o2, atol=1e-13) and np.allclose(lse, lse2, atol=1e-13)
+
+
+def test_linearity_in_v():
+    rng = np.random.default_rng(7)
+    q, k, v = _rand((1, 9, 2, 4), rng), _rand((1, 9, 2, 4), rng), _rand((1, 9, 2, 4), rng)
+    a, b = -1.7, 0.3
+    for causal in (False, True):
+        o, _ = oracle.attention(q, k, v, softmax_scale=0.6, causal=causal)
+        o2, _ = oracle.attention(q, k, a * v + b, softmax_scale=0.6, causal=causal)
+        assert np.allclose(o2, a * o + b, atol=1e-13)
+
+
+def test_key_shift_moves_lse_only():
+    rng = np.random.default_rng(8)
+    q, k, v = _rand((1, 7, 2, 5), rng), _rand((1, 7, 2, 5), rng), _rand((1, 7, 2, 5), rng)
+    c = rng.standard_normal(5)
+    scale = 0.9
+    for causal in (False, True):
+        o, lse = oracle.attention(q, k, v, softmax_scale=scale, causal=causal)
+        o2, lse2 = oracle.attention(q, k + c, v, softmax_scale=scale, causal=causal)
+        shift = scale * np.einsum("bihd,d->bhi", q, c)
+        assert np.allclose(o2, o, atol=1e-13)
+        assert np.allclose(lse2, lse + shift, atol=1e-13)
+
+
+def test_split_merge_identity():
+    rng = np.random.default_rng(9)
+    q, k, v = _rand((1, 4, 2, 8), rng), _rand((1, 23, 2, 8), rng), _rand((1, 23, 2, 8), rng)
+    o, lse = oracle.attention(q, k, v, softmax_scale=0.5)
+    cuts = [0, 5, 6, 17, 23]
+    parts = [oracle.attention(q, k[:, a:b], v[:, a:b], softmax_scale=0.5)
+             for a, b in zip(cuts[:-1], cuts[1:])]
+    om, lm = oracle.merge_partials([p[0] for p in parts],
+                                   [np.transpose(p[1], (0, 2, 1))[..., None].squeeze(-1)
+                                    for p in parts])
+    assert np.allclose(om, o, atol=1e-13)
+    assert np.allclose(lm, np.transpose(lse, (0, 2, 1)), atol=1e-13)
+
+
+def test_merge_with_empty_chunk():
+    o1 = np.array([[1.0, 2.0]])
+    l1 = np.array([0.5])
+    oe = np.zeros((1, 2))
+    le = np.array([-np.inf])
+    om, lm = oracle.merge_partials([o1, oe], [l1, le])
+    assert np.allclose(om, o1) and np.allclose(lm, l1)
+    om, lm = oracle.merge_partials([oe, oe], [le, le])
+    assert np.all(om == 0) and np.all(lm == -np.inf)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_matches_torch_sdpa_fp64(causal):
+    """Library cross-check: torch's fp64 CPU attention (top-left causal == ours when Sq == Sk)."""
+    rng = np.random.default_rng(10)
+    B, S, H, D = 2, 33, 3, 16
+    q, k, v = (torch.from_numpy(_rand((B, S, H, D), rng)) for _ in range(3))
+    scale = D ** -0.5
+    o, lse = oracle.attention(q, k, v, softmax_scale=scale, causal=causal)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        q.transpose(1, 2), k.transpose(1, 2), v.transpose(1, 2), is_causal=causal,
+        scale=scale).transpose(1, 2)
+    assert np.allclose(o, ref.numpy(), atol=1e-13)
+    s = torch.einsum("bihd,bjhd->bhij", q, k) * scale
+    if causal:
+        s = s.masked_fill(torch.ones(S, S, dtype=torch.bool).triu(1), -math.inf)
+    assert np.allclose(lse, torch.logsumexp(s, dim=-1).numpy(), atol=1e-13)
+
+
+def test_varlen_equals_per_sequence():
+    rng = np.random.default_rng(11)
+    sq = [3, 0, 5, 2]
+    sk = [4, 2, 5, 0]
+    H, D = 2, 4
+    cq = np.concatenate([[0], np.cumsum(sq)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(sk)]).astype(np.int32)
+    q, k, v = _rand((cq[-1], H, D), rng), _rand((ck[-1], H, D), rng), _rand((ck[-1], H, D), rng)
+    for causal in (False, True):
+        o, lse = oracle.attention(q, k, v, softmax_scale=0.5, causal=causal,
+                                  cu_seqlens_q=cq, cu_seqlens_k=ck)
+        for b in range(4):
+            if sq[b] == 0:
+                continue
+            qb = q[cq[b]:cq[b + 1]][None]
+            kb = k[ck[b]:ck[b + 1]][None]
+            vb = v[ck[b]:ck[b + 1]][None]
+            ob, lb = oracle.attention(qb, kb, vb, softmax_scale=0.5, causal=causal)
+            assert np.allclose(o[cq[b]:cq[b + 1]], ob[0], atol=1e-14)
+            assert np.array_equal(lse[:, cq[b]:cq[b + 1]], lb[0])
+
+
+def test_bf16_decoder_matches_torch():
+    rng = np.random.default_rng(12)
+    codes = rng.integers(0, 1 << 16, size=20000, dtype=np.uint16)
+    vals = torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.decode(codes, oracle.DT_BF16)
+    finite = np.isfinite(vals)
+    assert np.array_equal(got[finite], vals[finite])
+    assert np.array_equal(np.isnan(got), np.isnan(vals))
+
+
+def test_e4m3_decoder_matches_torch_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.decode(codes, oracle.DT_E4M3)
+    nan = np.isnan(vals)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(got[~nan], vals[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def test_fp8_descale_equals_dequantised_fp64():
+    from exact_attention_forward_gb300 import inputs
+    g = torch.Generator().manual_seed(13)
+    x = [torch.randn((1, 16, 2, 8), generator=g) for _ in range(3)]
+    qs = [inputs.quantize_e4m3(t) for t in x]
+    (q8, dq), (k8, dk), (v8, dv) = qs
+    o, lse = oracle.attention(q8, k8, v8, softmax_scale=0.3, descale=(dq, dk, dv))
+    deq = [t.to(torch.float64) * d for t, d in qs]
+    o2, lse2 = oracle.attention(*deq, softmax_scale=0.3)
+    assert np.allclose(o, o2, atol=1e-13) and np.allclose(lse, lse2, atol=1e-13)
+    # and descale really enters: q_descale scales the scores, v_descale the output
+    o3, _ = oracle.attention(q8, k8, v8, softmax_scale=0.3, descale=(dq, dk, 2 * dv))
+    assert np.allclose(o3, 2 * o, atol=1e-13)
+
+
+def test_rows_subset_equals_full():
+    rng = np.random.default_rng(14)
+    q, k, v = _rand((2, 10, 3, 4), rng), _rand((2, 10, 3, 4), rng), _rand((2, 10, 3, 4), rng)
+    o, lse = oracle.attention(q, k, v, softmax_scale=0.5, causal=True)
+    rows = np.array([[1, 2, 9], [0, 0, 0], [1, 0, 4]])
+    o_r, l_r = oracle.attention_rows(q, k, v, rows, softmax_scale=0.5, causal=True)
+    for r, (b, h, i) in enumerate(rows):
+        assert np.array_equal(o_r[r], o[b, i, h]) and l_r[r] == lse[b, h, i]
+
+
+def test_bad_arguments_rejected():
+    q = np.zeros((1, 2, 1, 4))
+    with pytest.raises(ValueError):
+        oracle.attention_rows(q, q, q, np.array([[0, 0, 5]]), softmax_scale=1.0)
+    with pytest.raises(ValueError):
+        oracle.attention_rows(q, q, q, np.array([[0, 3, 0]]), softmax_scale=1.0)
