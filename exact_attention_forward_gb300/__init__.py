@@ -1,0 +1,205 @@
+"""Attention forward pass for one GB300 (sm_103a) -- Python binding.
+
+Every step of the computation runs in the CUDA library ``_fa_gb300.so``
+(built from ``csrc/`` by ``_build.py``) behind the C ABI of ``include/fa.h``.
+This module only marshals arguments: it takes torch tensors for device memory
+and streams, allocates outputs with torch, and calls ``fa_fwd`` through
+ctypes.  There is no fallback: if the library is missing or the call fails,
+it raises.
+
+    o, lse = fwd(q, k, v, causal=True)
+
+q, k, v: CUDA tensors, bf16 or float8_e4m3fn, [B, S, H, D] (or packed
+[total, H, D] with cu_seqlens_q / cu_seqlens_k int32 [B + 1] on the device).
+Returns o (bf16, q's layout) and lse (fp32, [B, H, Sq] or [H, total_q]).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = ["fwd", "fa_fwd", "FaError", "workspace_size", "num_splits", "device_error",
+           "debug_set", "library_path", "EXPORTED_SYMBOLS", "load_library"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_fa_gb300.so")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_WORKSPACE, \
+    FA_ERR_DEVICE_TIMEOUT = range(6)
+FA_DTYPE_BF16, FA_DTYPE_E4M3 = 0, 1
+
+# Every function declared in include/fa.h.
+EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_num_splits", "fa_status_string",
+                    "fa_last_error_detail", "fa_device_error", "fa_debug_set")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"fa_fwd failed: status {status} ({detail})")
+        self.status = status
+        self.detail = detail
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"CUDA extension {_LIB_PATH} is missing; build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa_fwd.restype = i32
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, i32, i32, i32, i32,
+                               f32, i32, i32, vp, vp, vp, vp, sz, vp]
+        lib.fa_fwd_workspace_size.restype = sz
+        lib.fa_fwd_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.fa_fwd_num_splits.restype = i32
+        lib.fa_fwd_num_splits.argtypes = [i32, i32, i32, i32, i32]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_status_string.argtypes = [i32]
+        lib.fa_last_error_detail.restype = ctypes.c_char_p
+        lib.fa_last_error_detail.argtypes = []
+        lib.fa_device_error.restype = i32
+        lib.fa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+        lib.fa_debug_set.restype = None
+        lib.fa_debug_set.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
+        _lib = lib
+        return lib
+
+
+def _detail(lib) -> str:
+    d = lib.fa_last_error_detail()
+    return d.decode() if d else ""
+
+
+def fa_fwd(*args) -> int:
+    """Raw call of the C entry point (arguments exactly as in include/fa.h)."""
+    return load_library().fa_fwd(*args)
+
+
+def workspace_size(batch, heads, seqlen_q, seqlen_k, head_dim_v, causal=False) -> int:
+    return int(load_library().fa_fwd_workspace_size(batch, heads, seqlen_q, seqlen_k, head_dim_v,
+                                                    int(bool(causal))))
+
+
+def num_splits(batch, heads, seqlen_q, seqlen_k, causal=False) -> int:
+    return int(load_library().fa_fwd_num_splits(batch, heads, seqlen_q, seqlen_k,
+                                                int(bool(causal))))
+
+
+def device_error(clear: bool = True):
+    """(status, flags) of the device-side failure word; see fa_device_error."""
+    lib = load_library()
+    flags = ctypes.c_uint32(0)
+    st = lib.fa_device_error(ctypes.byref(flags), int(bool(clear)))
+    return st, flags.value
+
+
+def debug_set(wait_limit_ns: int = 0, inject: int = 0) -> None:
+    load_library().fa_debug_set(int(wait_limit_ns), int(inject))
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def fwd(q, k, v, *, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seqlens_k=None,
+        max_seqlen_q=None, max_seqlen_k=None, descale=None, workspace="auto", out=None,
+        lse=None, stream=None):
+    """Attention forward on the current CUDA device.  Returns (o, lse).
+
+    descale: for float8_e4m3fn inputs, (q, k, v) descales as python floats or
+    0-d fp32 CUDA tensors (None = 1.0).  workspace: "auto" (allocated with
+    torch when the shape benefits from splitting the key range), None (never
+    split) or a caller-owned uint8 CUDA tensor.
+    """
+    import torch
+
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dtype == torch.bfloat16:
+        dt = FA_DTYPE_BF16
+    elif q.dtype == torch.float8_e4m3fn:
+        dt = FA_DTYPE_E4M3
+    else:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype")
+    varlen = cu_seqlens_q is not None
+    if varlen:
+        total_q, heads, d = q.shape
+        total_k = k.shape[0]
+        dv = v.shape[2]
+        batch = cu_seqlens_q.numel() - 1
+        if max_seqlen_q is None or max_seqlen_k is None:
+            raise ValueError("varlen needs max_seqlen_q and max_seqlen_k")
+        sq_arg, sk_arg = total_q, total_k
+        o_shape = (total_q, heads, dv)
+        lse_shape = (heads, total_q)
+        mq, mk = int(max_seqlen_q), int(max_seqlen_k)
+    else:
+        batch, sq, heads, d = q.shape
+        sk = k.shape[1]
+        dv = v.shape[3]
+        sq_arg, sk_arg = sq, sk
+        o_shape = (batch, sq, heads, dv)
+        lse_shape = (batch, heads, sq)
+        mq, mk = sq, sk
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    dev = q.device
+    if out is None:
+        out = torch.empty(o_shape, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    ds = [None, None, None]
+    temps = []  # tensors made here that must outlive the kernel on `stream`
+    if dt == FA_DTYPE_E4M3 and descale is not None:
+        for i, x in enumerate(descale):
+            if x is None:
+                continue
+            if not isinstance(x, torch.Tensor):
+                x = torch.tensor(float(x), dtype=torch.float32, device=dev)
+                temps.append(x)
+            ds[i] = x
+    ws = None
+    ws_bytes = 0
+    if workspace == "auto":
+        if not varlen:
+            need = workspace_size(batch, heads, sq_arg, sk_arg, dv, causal)
+            if need > 0:
+                ws = torch.empty(need, dtype=torch.uint8, device=dev)
+                ws_bytes = need
+                temps.append(ws)
+    elif workspace is not None:
+        ws = workspace
+        ws_bytes = workspace.numel() * workspace.element_size()
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    st = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(batch), int(heads),
+                    int(sq_arg), int(sk_arg), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), mq, mk,
+                    int(d), int(dv), float(softmax_scale), int(bool(causal)), dt,
+                    _ptr(ds[0]), _ptr(ds[1]), _ptr(ds[2]), _ptr(ws), ws_bytes,
+                    ctypes.c_void_p(stream.cuda_stream))
+    if st != FA_OK:
+        raise FaError(st, _detail(lib))
+    for t in temps:
+        t.record_stream(stream)
+    return out, lse

@@ -1,0 +1,9 @@
+// Kernel instance: attention forward, bf16_d128 (see fa_fwd_kernel.cuh).
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+cudaError_t launch_fwd_bf16_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const FwdParams& p, int grid, cudaStream_t s) {
+    return launch_fwd<128, false>(q, k, v, p, grid, s);
+}
+}  // namespace fa

@@ -1,0 +1,9 @@
+// Kernel instance: attention forward, e4m3_d128 (see fa_fwd_kernel.cuh).
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+cudaError_t launch_fwd_e4m3_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const FwdParams& p, int grid, cudaStream_t s) {
+    return launch_fwd<128, true>(q, k, v, p, grid, s);
+}
+}  // namespace fa

@@ -1,0 +1,659 @@
+// fa_fwd_kernel.cuh -- the attention forward kernel for GB300 (sm_103a).
+//
+// Method (exact attention, computed block by block with an online softmax,
+// so S and P never leave the SM): "FlashAttention: Fast and Memory-Efficient
+// Exact Attention with IO-Awareness" (arXiv:2205.14135), as its forward pass
+// is walked through on the page "FlashAttention core algorithm: forward
+// pass" (inference.lei6393.com, flash_fwd_kernel_sm90.h excerpts):
+//   * a persistent tile-scheduler loop whose next work item is known before
+//     the epilogue runs (scheduler loop and "get_next_work before the
+//     epilogue" excerpts);
+//   * a producer that loads Q once per item and streams K/V blocks through
+//     full/empty pipelines (SharedStorage / PipelineStorage excerpt);
+//   * consumers that run the two GEMMs and the softmax with exp2 and a
+//     pre-multiplied softmax_scale_log2, FP8 descales folded into that scale,
+//     a running row maximum and row_sum, iterating key blocks from
+//     n_block_max - 1 down to n_block_min;
+//   * an epilogue that stores O and LSE, or zeros and -inf (store_zero).
+// The page "Dissecting the SM_120 Microarchitecture" (section 11.2, Fig. 12)
+// finds the softmax (exp2 on the SFU) rather than the MMAs to dominate a
+// key block on a GPU without TMEM, and lists overlapping MMA with softmax
+// across warps and keeping accumulators in Tensor Memory as the remedies;
+// both are the structure of this kernel.
+//
+// GB300 design (not a port of the pages' SM80/SM90 kernels):
+//   * 384 threads, one CTA per SM (persistent, grid = #SMs):
+//       warp 0      TMA producer (one elected thread)
+//       warp 1      TMEM allocator and tcgen05.mma issuer (one elected thread)
+//       warps 4-7   softmax + lazy correction + epilogue for query tile 0
+//       warps 8-11  the same for query tile 1
+//   * a work item is (batch, head, 256 query rows = two 128-row tiles, key
+//     split); both tiles consume every K/V block loaded, halving K/V traffic;
+//   * S_t = Q_t K^T and O_t += P_t V are tcgen05.mma (M=128) with fp32
+//     accumulators in TMEM: S_t at columns [128t, 128t+128), O_t at
+//     [256+128t, 256+128t+Dv); P_t (bf16 or e4m3) is written back over the
+//     first columns of S_t and fed to the PV MMA straight from TMEM;
+//   * the MMA issue order per key block j (reverse order) is
+//       PV_0(j), S_0(j-1), PV_1(j), S_1(j-1)
+//     so the tensor pipe works on one tile while the other tile's softmax
+//     runs (ping-pong); the tensor pipe executes one thread's MMAs in issue
+//     order, so S_t(j-1) overwriting P_t(j) after PV_t(j) is safe, and S_t(j)
+//     being complete implies PV_t(j+1) is complete -- which is what lets the
+//     softmax warps rescale O_t in place (lazily, only when the running max
+//     grows by more than 2^8) without a separate correction warpgroup;
+//   * every wait is bounded by wall clock; a timeout sets the device error
+//     word and all roles abandon the launch cleanly (TMEM released).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+constexpr int kBM = 128;          // query rows per tile (one TMEM lane per row)
+constexpr int kBN = 128;          // keys per K/V block
+constexpr int kTiles = 2;         // query tiles per work item
+constexpr int kThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kTau = 8.0f;      // lazy-rescale threshold (log2 units): p <= 2^8
+// Register split: launched at 168 per thread (384 x 168 = 64512); the producer /
+// MMA warpgroup gives up 48 per thread, the two softmax warpgroups take 24 more.
+constexpr uint32_t kRegsLoadMma = 120;
+constexpr uint32_t kRegsSoftmax = 192;
+static_assert(128 * kRegsLoadMma + 256 * kRegsSoftmax <= 384 * 168, "register split exceeds launch");
+
+template <int D, bool FP8>
+struct Cfg {
+    static constexpr int kElem = FP8 ? 1 : 2;
+    static constexpr int kRowBytes = D * kElem;
+    static constexpr int kChunks = kRowBytes / 128;        // 128-byte swizzle atoms per row
+    static constexpr int kChunkElems = 128 / kElem;
+    static constexpr int kChunkBytes = kBM * 128;          // one atom column of a tile: 16 KiB
+    static constexpr int kTileBytes = kBM * kRowBytes;     // Q tile == K/V block (BM == BN)
+    static constexpr int kUmmaK = 32 / kElem;              // reduction depth of one MMA
+    static constexpr int kStages = (FP8 || D == 64) ? 8 : 4;
+    static constexpr int kPCols = kBN * kElem / 4;         // TMEM columns of a P tile
+    static constexpr int kQOff = 0;
+    static constexpr int kKVOff = kTiles * kTileBytes;
+    static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+    enum {
+        Q_FULL = 0, Q_EMPTY = 2, S_FULL = 4, P_FULL = 6, O_FULL = 8, O_EMPTY = 10, DRAIN = 12,
+        KV_FULL = 13, KV_EMPTY = 13 + kStages, NUM_BARS = 13 + 2 * kStages
+    };
+    static constexpr int kMiscOff = kBarOff + NUM_BARS * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1 KiB
+    static constexpr uint32_t kIdescQK = make_idesc(kBM, kBN, 0u + (FP8 ? 0u : 1u), false);
+    static constexpr uint32_t kIdescPV = make_idesc(kBM, D, 0u + (FP8 ? 0u : 1u), true);
+    static constexpr uint32_t kColO = 256;
+    static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle atoms");
+    static_assert(kSmemBytes <= 232448, "exceeds the 227 KiB per-block shared memory");
+    static_assert(kSmemBytes > 232448 / 2, "must keep one CTA (and one 512-column TMEM) per SM");
+};
+
+// One unit of work: a pair of 128-row query tiles of one (batch, head) and a
+// range of key blocks.  Decoded identically by every role from its index.
+struct Item {
+    int b, h, split;
+    int sq, sk;          // this sequence's lengths
+    int q_row0, k_row0;  // first row of this sequence in the packed / fixed tensors
+    int m0[kTiles];      // first query row (within the sequence) of each tile
+    int n_lo, n_hi;      // key blocks [n_lo, n_hi) are visited, in reverse
+    int n_hi_t[kTiles];  // tile t visits [n_lo, n_hi_t[t]); none if n_hi_t[t] <= n_lo
+    bool active[kTiles]; // tile t has at least one row inside the sequence
+};
+
+// Longest-processing-time order: item index -> pair index descending (under a
+// causal mask later pairs see more key blocks), then (batch, head, split).
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int w) {
+    Item it;
+    const int per_m = p.batch * p.heads * p.n_splits;
+    const int mp = p.n_mpairs - 1 - w / per_m;
+    const int r = w % per_m;
+    it.split = r % p.n_splits;
+    const int bh = r / p.n_splits;
+    it.h = bh % p.heads;
+    it.b = bh / p.heads;
+    if (p.varlen) {
+        it.q_row0 = __ldg(p.cu_q + it.b);
+        it.sq = __ldg(p.cu_q + it.b + 1) - it.q_row0;
+        it.k_row0 = __ldg(p.cu_k + it.b);
+        it.sk = __ldg(p.cu_k + it.b + 1) - it.k_row0;
+    } else {
+        it.q_row0 = it.b * p.seqlen_q;
+        it.sq = p.seqlen_q;
+        it.k_row0 = it.b * p.seqlen_k;
+        it.sk = p.seqlen_k;
+    }
+    const int nblk = (it.sk + kBN - 1) / kBN;
+    it.n_lo = it.split * p.blocks_per_split;
+    const int n_end = min(nblk, it.n_lo + p.blocks_per_split);
+    it.n_hi = it.n_lo;
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t) {
+        it.m0[t] = mp * (kTiles * kBM) + t * kBM;
+        it.active[t] = it.m0[t] < it.sq;
+        int hi = n_end;
+        if (p.causal) {
+            const int rmax = min(it.m0[t] + kBM, it.sq) - 1;
+            const int last = rmax + it.sk - it.sq;  // last visible key of the tile's last row
+            hi = last < 0 ? 0 : min(hi, last / kBN + 1);
+        }
+        if (!it.active[t]) hi = it.n_lo;
+        it.n_hi_t[t] = max(hi, it.n_lo);
+        it.n_hi = max(it.n_hi, it.n_hi_t[t]);
+    }
+    return it;
+}
+
+// Snake-ordered static assignment of items to persistent CTAs: round r hands
+// items [r*G, (r+1)*G) to the CTAs in forward order on even rounds and in
+// reverse order on odd ones, which balances the descending item costs.
+__device__ __forceinline__ int item_of_round(int round, int nctas) {
+    const int pos = (round & 1) ? (nctas - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+    return round * nctas + pos;
+}
+
+struct WaitCtx {
+    uint64_t limit_ns;
+    uint32_t* err;
+    volatile uint32_t* abort_flag;  // shared memory
+};
+
+static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                       uint32_t site) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 128; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*w.abort_flag) return false;
+        if (globaltimer_ns() - t0 > w.limit_ns) {
+            atomicCAS(w.err, 0u, kErrTimeout | (site << 8));
+            atomicOr(w.err, kErrTimeout);
+            *w.abort_flag = 1u;
+            __threadfence_block();
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                         uint32_t site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, w, site);
+}
+
+// Wait-site codes reported in bits 8..15 of the error word.
+enum : uint32_t {
+    SITE_Q_EMPTY = 1, SITE_KV_EMPTY = 2, SITE_Q_FULL = 3, SITE_KV_FULL = 4, SITE_P_FULL = 5,
+    SITE_O_EMPTY = 6, SITE_S_FULL = 7, SITE_O_FULL = 8, SITE_DRAIN = 9
+};
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    using C = Cfg<D, FP8>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t s_q = s_base + C::kQOff;
+    const uint32_t s_kv = s_base + C::kKVOff;
+    const uint32_t s_bar = s_base + C::kBarOff;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
+    auto bar = [&](int i) -> uint32_t { return s_bar + 8u * (uint32_t)i; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < kTiles; ++t) {
+            mbar_init(bar(C::Q_FULL + t), 1);
+            mbar_init(bar(C::Q_EMPTY + t), 1);
+            mbar_init(bar(C::S_FULL + t), 1);
+            mbar_init(bar(C::P_FULL + t), kBM);
+            mbar_init(bar(C::O_FULL + t), 1);
+            mbar_init(bar(C::O_EMPTY + t), kBM);
+        }
+        mbar_init(bar(C::DRAIN), 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar(C::KV_FULL + s), 1);
+            mbar_init(bar(C::KV_EMPTY + s), 1);
+        }
+        *abort_flag = 0u;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const WaitCtx wc{p.wait_limit_ns, p.err, abort_flag};
+    const int nctas = (int)gridDim.x;
+
+    if (warp < 4) {
+    setmaxnreg_dec<kRegsLoadMma>();
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            const uint64_t pol_q = l2_policy_evict_first();
+            const uint64_t pol_kv = l2_policy_evict_last();
+            uint32_t ring = 0, q_cnt[kTiles] = {0, 0};
+            bool withheld = false;
+            bool aborted = false;
+            for (int round = 0; !aborted; ++round) {
+                const int w = item_of_round(round, nctas);
+                if (w >= p.n_items) break;
+                const Item it = decode_item(p, w);
+                if (it.n_hi <= it.n_lo) continue;
+                const int qb = p.varlen ? 0 : it.b;
+                const int kb = qb;
+                for (int t = 0; t < kTiles && !aborted; ++t) {
+                    if (it.n_hi_t[t] <= it.n_lo) continue;
+                    if (!wait_bar(bar(C::Q_EMPTY + t), (q_cnt[t] & 1u) ^ 1u, wc, SITE_Q_EMPTY)) {
+                        aborted = true;
+                        break;
+                    }
+                    ++q_cnt[t];
+                    if (p.inject == 1u && !withheld) {  // debug: never arrive on this Q tile
+                        withheld = true;
+                        continue;
+                    }
+                    const int qrow = (p.varlen ? it.q_row0 : 0) + it.m0[t];
+                    mbar_arrive_expect_tx(bar(C::Q_FULL + t), C::kTileBytes);
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_4d(s_q + t * C::kTileBytes + c * C::kChunkBytes, &tm_q,
+                                    bar(C::Q_FULL + t), c * C::kChunkElems, it.h, qrow, qb, pol_q);
+                }
+                for (int j = it.n_hi - 1; j >= it.n_lo && !aborted; --j) {
+                    const int krow = (p.varlen ? it.k_row0 : 0) + j * kBN;
+#pragma unroll 1
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const uint32_t slot = ring % C::kStages;
+                        const uint32_t ph = (ring / C::kStages) & 1u;
+                        if (!wait_bar(bar(C::KV_EMPTY + slot), ph ^ 1u, wc, SITE_KV_EMPTY)) {
+                            aborted = true;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bar(C::KV_FULL + slot), C::kTileBytes);
+#pragma unroll
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_4d(s_kv + slot * C::kTileBytes + c * C::kChunkBytes,
+                                        kv ? &tm_v : &tm_k, bar(C::KV_FULL + slot),
+                                        c * C::kChunkElems, it.h, krow, kb, pol_kv);
+                        ++ring;
+                    }
+                }
+            }
+            if (aborted) {  // let copies already in flight land before the CTA retires
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 200000ull) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t ring = 0, q_cnt[kTiles] = {0, 0}, p_cnt[kTiles] = {0, 0},
+                     o_cnt[kTiles] = {0, 0};
+            bool aborted = false;
+            // S_t = Q_t K^T : A = Q (K-major), B = K (K-major), both 128B-swizzled.
+            auto issue_qk = [&](int t, uint32_t kslot) {
+                const uint32_t q_addr = s_q + t * C::kTileBytes;
+                const uint32_t k_addr = s_kv + kslot * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / C::kUmmaK; ++kk) {
+                    const int c = kk * C::kUmmaK / C::kChunkElems;
+                    const int sub = (kk * 32) % 128;  // byte offset inside the 128-byte atom row
+                    const uint64_t a = sdesc_sw128(q_addr + c * C::kChunkBytes + sub, 16, 1024);
+                    const uint64_t b = sdesc_sw128(k_addr + c * C::kChunkBytes + sub, 16, 1024);
+                    if constexpr (FP8)
+                        umma_f8_ss(tmem_base + 128u * t, a, b, C::kIdescQK, kk > 0);
+                    else
+                        umma_f16_ss(tmem_base + 128u * t, a, b, C::kIdescQK, kk > 0);
+                }
+            };
+            // O_t += P_t V : A = P_t from TMEM, B = V (MN-major, 128B-swizzled):
+            // leading offset = next 128-byte column atom, stride offset = next 8 keys.
+            auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
+                const uint32_t v_addr = s_kv + vslot * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBN / C::kUmmaK; ++kk) {
+                    const uint64_t b = sdesc_sw128(v_addr + kk * C::kUmmaK * 128, C::kChunkBytes, 1024);
+                    const uint32_t a_tmem = tmem_base + 128u * t + 8u * kk;
+                    if constexpr (FP8)
+                        umma_f8_ts(tmem_base + C::kColO + 128u * t, a_tmem, b, C::kIdescPV,
+                                   (acc || kk > 0) ? 1u : 0u);
+                    else
+                        umma_f16_ts(tmem_base + C::kColO + 128u * t, a_tmem, b, C::kIdescPV,
+                                    (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            for (int round = 0; !aborted; ++round) {
+                const int w = item_of_round(round, nctas);
+                if (w >= p.n_items) break;
+                const Item it = decode_item(p, w);
+                if (it.n_hi <= it.n_lo) continue;
+                for (int t = 0; t < kTiles; ++t) {
+                    if (it.n_hi_t[t] <= it.n_lo) continue;
+                    if (!wait_bar(bar(C::Q_FULL + t), q_cnt[t] & 1u, wc, SITE_Q_FULL)) {
+                        aborted = true;
+                        break;
+                    }
+                }
+                if (aborted) break;
+                tc_fence_after();
+                bool first[kTiles] = {true, true};
+                const int j0 = it.n_hi - 1;
+                uint32_t kslot = ring % C::kStages;
+                if (!wait_bar(bar(C::KV_FULL + kslot), (ring / C::kStages) & 1u, wc, SITE_KV_FULL)) {
+                    aborted = true;
+                    break;
+                }
+                ++ring;
+                for (int t = 0; t < kTiles; ++t) {
+                    if (j0 < it.n_hi_t[t]) {
+                        issue_qk(t, kslot);
+                        umma_commit(bar(C::S_FULL + t));
+                    }
+                }
+                umma_commit(bar(C::KV_EMPTY + kslot));
+                for (int j = j0; j >= it.n_lo && !aborted; --j) {
+                    const uint32_t vslot = ring % C::kStages;
+                    if (!wait_bar(bar(C::KV_FULL + vslot), (ring / C::kStages) & 1u, wc, SITE_KV_FULL)) {
+                        aborted = true;
+                        break;
+                    }
+                    ++ring;
+                    const bool has_next = j - 1 >= it.n_lo;
+                    uint32_t nslot = 0, nph = 0;
+                    bool next_ready = false;
+                    if (has_next) {
+                        nslot = ring % C::kStages;
+                        nph = (ring / C::kStages) & 1u;
+                        ++ring;
+                    }
+                    for (int t = 0; t < kTiles; ++t) {
+                        const bool cur = j < it.n_hi_t[t];
+                        const bool nxt = has_next && (j - 1) < it.n_hi_t[t];
+                        if (cur) {
+                            if (!wait_bar(bar(C::P_FULL + t), p_cnt[t] & 1u, wc, SITE_P_FULL)) {
+                                aborted = true;
+                                break;
+                            }
+                            ++p_cnt[t];
+                            if (first[t] &&
+                                !wait_bar(bar(C::O_EMPTY + t), (o_cnt[t] & 1u) ^ 1u, wc, SITE_O_EMPTY)) {
+                                aborted = true;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_pv(t, vslot, !first[t]);
+                            first[t] = false;
+                        }
+                        if (nxt) {
+                            if (!next_ready) {
+                                if (!wait_bar(bar(C::KV_FULL + nslot), nph, wc, SITE_KV_FULL)) {
+                                    aborted = true;
+                                    break;
+                                }
+                                next_ready = true;
+                            }
+                            issue_qk(t, nslot);
+                            umma_commit(bar(C::S_FULL + t));
+                        } else if (cur) {
+                            umma_commit(bar(C::O_FULL + t));  // last block of tile t
+                        }
+                    }
+                    if (aborted) break;
+                    umma_commit(bar(C::KV_EMPTY + vslot));
+                    if (has_next) umma_commit(bar(C::KV_EMPTY + nslot));
+                }
+                if (aborted) break;
+                for (int t = 0; t < kTiles; ++t) {
+                    if (it.n_hi_t[t] <= it.n_lo) continue;
+                    umma_commit(bar(C::Q_EMPTY + t));
+                    ++q_cnt[t];
+                    ++o_cnt[t];
+                }
+            }
+            // Drain: every MMA issued by this thread has completed before TMEM is released.
+            umma_commit(bar(C::DRAIN));
+            wait_bar(bar(C::DRAIN), 0u, wc, SITE_DRAIN);
+        }
+        __syncwarp();
+    }
+    } else {
+        setmaxnreg_inc<kRegsSoftmax>();
+        // ------------------------------------------------------------ softmax / epilogue
+        const int t = (warp - 4) >> 2;              // query tile of this warpgroup
+        const int wq = warp & 3;                    // TMEM lane quarter of this warp
+        const int r_in_tile = wq * 32 + lane;       // this thread's row within the tile
+        const uint32_t t_lane = tmem_base + ((uint32_t)(wq * 32) << 16);
+        const uint32_t t_s = t_lane + 128u * t;     // S_t (fp32) and, over it, P_t
+        const uint32_t t_o = t_lane + C::kColO + 128u * t;
+        float scale_log2 = p.scale_log2;
+        float o_scale = 1.0f;
+        if constexpr (FP8) {
+            const float qd = p.q_descale ? __ldg(p.q_descale) : 1.0f;
+            const float kd = p.k_descale ? __ldg(p.k_descale) : 1.0f;
+            scale_log2 *= qd * kd;
+            o_scale = p.v_descale ? __ldg(p.v_descale) : 1.0f;
+        }
+        uint32_t s_cnt = 0, o_cnt = 0;
+        bool aborted = false;
+        for (int round = 0; !aborted; ++round) {
+            const int w = item_of_round(round, nctas);
+            if (w >= p.n_items) break;
+            const Item it = decode_item(p, w);
+            if (!it.active[t]) continue;
+            const int row = it.m0[t] + r_in_tile;  // row within the sequence
+            const bool row_ok = row < it.sq;
+            // output addresses
+            float* lse_ptr;
+            float* wso_ptr = nullptr;
+            __nv_bfloat16* o_ptr = nullptr;
+            if (p.split) {
+                const size_t rid =
+                    (((size_t)it.split * p.batch + it.b) * p.heads + it.h) * (size_t)p.seqlen_q + row;
+                lse_ptr = p.ws_lse + rid;
+                wso_ptr = p.ws_o + rid * D;
+            } else if (p.varlen) {
+                lse_ptr = p.lse + (size_t)it.h * p.total_q + it.q_row0 + row;
+                o_ptr = reinterpret_cast<__nv_bfloat16*>(p.o) +
+                        (((size_t)it.q_row0 + row) * p.heads + it.h) * D;
+            } else {
+                lse_ptr = p.lse + ((size_t)it.b * p.heads + it.h) * p.seqlen_q + row;
+                o_ptr = reinterpret_cast<__nv_bfloat16*>(p.o) +
+                        (((size_t)it.b * p.seqlen_q + row) * p.heads + it.h) * D;
+            }
+            if (it.n_hi_t[t] <= it.n_lo) {
+                // no visible key for any row of this tile: O = 0, LSE = -inf
+                if (row_ok) {
+                    if (p.split) {
+                        for (int c = 0; c < D; c += 4)
+                            *reinterpret_cast<float4*>(wso_ptr + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    } else {
+                        for (int c = 0; c < D; c += 8)
+                            *reinterpret_cast<uint4*>(o_ptr + c) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    *lse_ptr = -INFINITY;
+                }
+                continue;
+            }
+            // visible keys of this row: [0, vis_end) with vis_end = min(sk, row + sk - sq + 1)
+            const int vis_end = p.causal ? min(it.sk, row + it.sk - it.sq + 1) : it.sk;
+            // a block needs masking iff some column of it is invisible to some row of the tile
+            const int tile_rmin = it.m0[t];
+            const int tile_vis_min = p.causal ? min(it.sk, tile_rmin + it.sk - it.sq + 1) : it.sk;
+            float m_run = -INFINITY;  // running max of scale_log2 * s (lazy reference)
+            float l_run = 0.0f;       // running sum of exp2(scale_log2 * s - m_run)
+            const int j_first = it.n_hi_t[t] - 1;
+            for (int j = j_first; j >= it.n_lo; --j) {
+                bool ok = wait_bar(bar(C::S_FULL + t), s_cnt & 1u, wc, SITE_S_FULL);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    aborted = true;
+                    break;
+                }
+                ++s_cnt;
+                tc_fence_after();
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) tmem_ld32(t_s + 32u * q, sr[q]);
+                tmem_wait_ld();
+                float s[128];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[q * 32 + i] = __uint_as_float(sr[q][i]);
+                const int col0 = j * kBN;
+                if (col0 + kBN > tile_vis_min) {  // diagonal or key-tail block
+                    const int lim = vis_end - col0;
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c >= lim) s[c] = -INFINITY;
+                }
+                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int c = 4; c < 128; c += 4) {
+                    mx0 = fmaxf(mx0, s[c]);
+                    mx1 = fmaxf(mx1, s[c + 1]);
+                    mx2 = fmaxf(mx2, s[c + 2]);
+                    mx3 = fmaxf(mx3, s[c + 3]);
+                }
+                const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
+                if (m_cand > m_run + kTau) {
+                    // the reference max grows: rescale l and (except on the first block,
+                    // whose PV overwrites O) the accumulated O of this row.
+                    const float f = ex2_approx(m_run - m_cand);  // 0 when m_run = -inf
+                    if (j != j_first && m_run != -INFINITY) {
+#pragma unroll 1
+                        for (int c = 0; c < D; c += 16) {
+                            uint32_t orr[16];
+                            tmem_ld16(t_o + c, orr);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                orr[i] = __float_as_uint(__uint_as_float(orr[i]) * f);
+                            tmem_st16(t_o + c, orr);
+                        }
+                    }
+                    l_run *= f;
+                    m_run = m_cand;
+                }
+                const float mu = (m_run == -INFINITY) ? 0.0f : m_run;
+                float ls0 = 0.f, ls1 = 0.f;
+                if constexpr (FP8) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 128; c += 4) {
+                        const float e0 = ex2_approx(fmaf(s[c], scale_log2, -mu));
+                        const float e1 = ex2_approx(fmaf(s[c + 1], scale_log2, -mu));
+                        const float e2 = ex2_approx(fmaf(s[c + 2], scale_log2, -mu));
+                        const float e3 = ex2_approx(fmaf(s[c + 3], scale_log2, -mu));
+                        ls0 += e0 + e2;
+                        ls1 += e1 + e3;
+                        pk[c / 4] = pack_e4m3x4(e0, e1, e2, e3);
+                    }
+                    tmem_st32(t_s, pk);
+                } else {
+                    uint32_t pk[64];
+#pragma unroll
+                    for (int c = 0; c < 128; c += 2) {
+                        const float e0 = ex2_approx(fmaf(s[c], scale_log2, -mu));
+                        const float e1 = ex2_approx(fmaf(s[c + 1], scale_log2, -mu));
+                        ls0 += e0;
+                        ls1 += e1;
+                        pk[c / 2] = pack_bf16x2(e0, e1);
+                    }
+                    tmem_st32(t_s, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+                    tmem_st32(t_s + 32u, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+                }
+                l_run += ls0 + ls1;
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(C::P_FULL + t));
+            }
+            if (aborted) break;
+            // ---------------- epilogue: O = O_acc / l, LSE = ln2 * (m + log2 l)
+            {
+                bool ok = wait_bar(bar(C::O_FULL + t), o_cnt & 1u, wc, SITE_O_FULL);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    aborted = true;
+                    break;
+                }
+                ++o_cnt;
+            }
+            tc_fence_after();
+            const bool has_mass = l_run > 0.0f;
+            const float inv_l = has_mass ? o_scale / l_run : 0.0f;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t orr[32];
+                tmem_ld32(t_o + c, orr);
+                tmem_wait_ld();
+                if (row_ok) {
+                    if (p.split) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4*>(wso_ptr + c + i) = make_float4(
+                                __uint_as_float(orr[i]) * inv_l, __uint_as_float(orr[i + 1]) * inv_l,
+                                __uint_as_float(orr[i + 2]) * inv_l, __uint_as_float(orr[i + 3]) * inv_l);
+                    } else {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
+                                                __uint_as_float(orr[2 * i + 1]) * inv_l);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            *reinterpret_cast<uint4*>(o_ptr + c + 8 * i) =
+                                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(C::O_EMPTY + t));
+            if (row_ok)
+                *lse_ptr = has_mass ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <int D, bool FP8>
+cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const FwdParams& p, int grid, cudaStream_t stream) {
+    using C = Cfg<D, FP8>;
+    static bool attr_done = false;  // per process; the attribute is per function
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, FP8>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    fa_fwd_kernel<D, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, p);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,137 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) attention forward library.
+ *
+ * The operation is the exact attention forward pass described by the page
+ * "FlashAttention core algorithm: forward pass" (inference.lei6393.com,
+ * FlashAttention 02-core-algorithm / 03-forward-pass): for each query row the
+ * consumer mainloop accumulates softmax(scale * Q K^T) V block by block over
+ * K/V with a running row maximum and row sum, using exp2 with a pre-multiplied
+ * softmax_scale_log2 (consumer excerpt, step 1), folds the FP8 q/k descales
+ * into that scale (same excerpt, FP8 branch), and the epilogue writes O and
+ * the per-row log-sum-exp, or all-zero O and -inf LSE for rows that see no
+ * key (epilogue excerpt, store / store_zero).  The algorithm itself is the
+ * one of "FlashAttention: Fast and Memory-Efficient Exact Attention with
+ * IO-Awareness" (arXiv:2205.14135), which the page "FlashAttention SM120
+ * forward reuses the SM80 mainloop" (xuesongtap.github.io) cites as its
+ * background (reference [8]).
+ *
+ * Per query row i of head h in batch b, with visible key set V_i:
+ *     O_i   = sum_{j in V_i} softmax_j(scale * q_i . k_j) v_j
+ *     LSE_i = ln sum_{j in V_i} exp(scale * q_i . k_j)
+ * V_i = all keys, or with causal = 1, {j : j <= i + Sk - Sq} (bottom-right
+ * aligned).  V_i empty => O_i = 0 and LSE_i = -inf, never NaN.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
+ *    aligned.  The library allocates no device memory, never synchronises the
+ *    stream, and keeps only host-side caches.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *  - Every argument is validated before anything is launched; on a non-OK
+ *    status nothing has been written and fa_last_error_detail() says why.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,     /* NULL/misaligned pointer, negative size, bad scale, ... */
+    FA_ERR_UNSUPPORTED = 2,     /* valid but not built: head_dim not in {64,128}, ... */
+    FA_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed (launch, tensor map) */
+    FA_ERR_WORKSPACE = 4,       /* workspace given but smaller than fa_fwd_workspace_size() */
+    FA_ERR_DEVICE_TIMEOUT = 5   /* a bounded device-side wait gave up (see fa_device_error) */
+} fa_status;
+
+typedef enum {
+    FA_DTYPE_BF16 = 0,          /* Q, K, V bfloat16 */
+    FA_DTYPE_E4M3 = 1           /* Q, K, V float8 e4m3 (OCP "fn"), per-tensor descales */
+} fa_dtype;
+
+/*
+ * fa_fwd -- attention forward pass.
+ *
+ * Layouts (row-major, contiguous):
+ *   fixed length (cu_seqlens_q == cu_seqlens_k == NULL):
+ *     q [batch, seqlen_q, heads, head_dim]      k, v [batch, seqlen_k, heads, head_dim]
+ *     o [batch, seqlen_q, heads, head_dim_v] bf16
+ *     lse [batch, heads, seqlen_q] fp32
+ *   packed variable length (both cu_seqlens given; device int32 [batch + 1],
+ *   non-decreasing, cu[0] = 0):
+ *     q [seqlen_q, heads, head_dim]  where seqlen_q = cu_seqlens_q[batch] (total rows)
+ *     k, v [seqlen_k, heads, head_dim] where seqlen_k = cu_seqlens_k[batch]
+ *     o [seqlen_q, heads, head_dim_v] bf16,  lse [heads, seqlen_q] fp32
+ *     max_seqlen_q / max_seqlen_k bound every sequence's length; a sequence may
+ *     have zero query rows or zero keys (its rows then get O = 0, LSE = -inf).
+ * batch, heads >= 1 (batch == 0 or seqlen_q == 0: FA_OK, nothing launched).
+ * head_dim == head_dim_v in {64, 128}; other values: FA_ERR_UNSUPPORTED.
+ * softmax_scale: finite, > 0 (typically 1/sqrt(head_dim)).
+ * causal: 0 or 1.
+ * dtype FA_DTYPE_E4M3: q/k/v_descale are device fp32 scalars (NULL means 1.0);
+ *   scores use softmax_scale * q_descale * k_descale and O is multiplied by
+ *   v_descale.  Descale pointers must be NULL for FA_DTYPE_BF16.
+ * workspace: optional device scratch for splitting long key ranges over
+ *   several CTAs (short-query / long-key shapes).  NULL disables splitting.
+ *   If non-NULL it must hold fa_fwd_workspace_size(...) bytes, else
+ *   FA_ERR_WORKSPACE.  Fixed-length inputs only; ignored for varlen.
+ * stream: cudaStream_t.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v,
+                 void* o, float* lse,
+                 int batch, int heads, int seqlen_q, int seqlen_k,
+                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                 int max_seqlen_q, int max_seqlen_k,
+                 int head_dim, int head_dim_v, float softmax_scale, int causal,
+                 fa_dtype dtype,
+                 const float* q_descale, const float* k_descale, const float* v_descale,
+                 void* workspace, size_t workspace_bytes,
+                 void* stream);
+
+/*
+ * Bytes of workspace that fa_fwd would use to split the key range of a
+ * fixed-length problem of this shape on the current device (0 = it would not
+ * split).  Splitting follows the log-sum-exp merge identity: each split
+ * writes a normalised partial O and its LSE, a second kernel merges them.
+ */
+size_t fa_fwd_workspace_size(int batch, int heads, int seqlen_q, int seqlen_k,
+                             int head_dim_v, int causal);
+
+/* Number of key splits fa_fwd would use for that shape with a workspace. */
+int fa_fwd_num_splits(int batch, int heads, int seqlen_q, int seqlen_k, int causal);
+
+/* Static description of a status code. */
+const char* fa_status_string(fa_status status);
+
+/* Thread-local message describing the last non-OK status of this thread. */
+const char* fa_last_error_detail(void);
+
+/*
+ * Device-side failure detection.  Every wait inside the kernels is bounded
+ * (by wall clock, default 4 s).  A wait that runs out sets a bit in a
+ * device-resident error word, the kernel's CTAs abandon their work and exit
+ * cleanly (TMEM released), and the context stays usable.
+ * fa_device_error synchronises the current device, copies the word to
+ * *flags (bit 0: a wait timed out; bits 8..15: the site of the first
+ * timeout) and, if clear != 0, resets it.  Returns FA_ERR_DEVICE_TIMEOUT if
+ * a timeout bit was set, FA_OK otherwise (FA_ERR_CUDA on a CUDA failure).
+ */
+fa_status fa_device_error(uint32_t* flags, int clear);
+
+/*
+ * Debug controls for the failure-detection tests (process-wide, host side,
+ * applied to subsequent launches).  wait_limit_ns = 0 restores the default.
+ * inject: 0 = none; 1 = the TMA producer withholds the first Q-tile arrival
+ * of each CTA, so the MMA issuer's bounded wait runs out (no GPU fault).
+ */
+void fa_debug_set(uint64_t wait_limit_ns, uint32_t inject);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

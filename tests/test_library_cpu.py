@@ -1,0 +1,83 @@
+"""CPU-only checks of the CUDA library: it builds, loads without a GPU and
+exports every function include/fa.h declares; argument validation that runs
+before any device work returns the documented codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_forward_gb300 as fa
+from exact_attention_forward_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return fa.load_library()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert header_functions() == sorted(fa.EXPORTED_SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.fa_status_string(code)
+    assert b"unknown" in lib.fa_status_string(99)
+
+
+# a fake, 16-byte aligned address: validation never dereferences pointers
+P = ctypes.c_void_p(0x10000)
+
+
+def call(lib, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, batch=1, heads=1, sq=128, sk=128, cuq=None, cuk=None,
+             mq=0, mk=0, d=128, dv=128, scale=0.1, causal=0, dtype=0, qd=None, kd=None, vd=None,
+             ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return lib.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["batch"], a["heads"], a["sq"],
+                      a["sk"], a["cuq"], a["cuk"], a["mq"], a["mk"], a["d"], a["dv"], a["scale"],
+                      a["causal"], a["dtype"], a["qd"], a["kd"], a["vd"], a["ws"], a["wsb"],
+                      a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(o=ctypes.c_void_p(0x10008)), fa.FA_ERR_INVALID_ARG),
+    (dict(heads=0), fa.FA_ERR_INVALID_ARG),
+    (dict(batch=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(sq=-5), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=2), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
+    (dict(qd=P), fa.FA_ERR_INVALID_ARG),             # descale with bf16
+    (dict(cuq=P), fa.FA_ERR_INVALID_ARG),            # only one cu_seqlens
+    (dict(d=96, dv=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=128, dv=64), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=64, dv=64, dtype=1), fa.FA_ERR_UNSUPPORTED),
+])
+def test_validation_codes(lib, kw, code):
+    assert call(lib, **kw) == code
+    assert lib.fa_last_error_detail()
+
+
+def test_empty_problems_are_ok_without_a_device(lib):
+    assert call(lib, batch=0) == fa.FA_OK
+    assert call(lib, sq=0) == fa.FA_OK

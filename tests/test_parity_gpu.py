@@ -1,0 +1,226 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs, element by element.
+
+Small shapes are compared in full (several tiles plus ragged tails in both
+the query and key directions); the full-size workloads are compared on
+sampled rows (every tile boundary of every (batch, head) plus random rows),
+run in the same launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import exact_attention_forward_gb300 as fa
+from exact_attention_forward_gb300 import inputs
+from parity_util import compare, gather_rows, run_gpu, sample_rows, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    fa.debug_set(0, 0)
+    fa.device_error(clear=True)
+
+
+SMALL = [
+    # B, H, Sq, Sk, D, causal
+    (1, 1, 128, 128, 128, False),
+    (1, 1, 128, 128, 128, True),
+    (2, 3, 1, 1, 64, False),
+    (1, 2, 127, 129, 128, False),
+    (1, 2, 129, 127, 128, True),
+    (2, 2, 255, 300, 64, True),
+    (1, 1, 513, 257, 128, False),
+    (1, 2, 300, 513, 128, True),   # Sq < Sk: bottom-right diagonal
+    (1, 2, 513, 300, 128, True),   # Sq > Sk: leading rows see no key
+    (1, 1, 3, 1000, 128, False),
+    (1, 4, 384, 384, 64, True),
+    (3, 2, 640, 640, 128, True),
+    (1, 1, 1024, 1024, 128, False),
+]
+
+
+@pytest.mark.parametrize("B,H,Sq,Sk,D,causal", SMALL)
+def test_small_shapes_full(B, H, Sq, Sk, D, causal):
+    x = inputs.make_random(B, H, Sq, Sk, D, seed=17 + Sq + 3 * Sk + D)
+    scale = D ** -0.5
+    o, lse = run_gpu(x, causal=causal, softmax_scale=scale)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=scale, causal=causal)
+    compare(o, lse, o_ref, lse_ref, what=f"{(B, H, Sq, Sk, D, causal)}")
+
+
+def test_bf16_small_workload_full():
+    w = inputs.WORKLOADS["bf16_small"]
+    x = inputs.make_inputs(w)
+    o, lse = run_gpu(x, causal=w.causal, softmax_scale=w.softmax_scale)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=w.softmax_scale,
+                                      causal=w.causal)
+    compare(o, lse, o_ref, lse_ref, what=w.name)
+
+
+def test_bf16_causal_2k_workload_full():
+    w = inputs.WORKLOADS["bf16_causal_2k"]
+    x = inputs.make_inputs(w)
+    o, lse = run_gpu(x, causal=w.causal, softmax_scale=w.softmax_scale)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=w.softmax_scale,
+                                      causal=w.causal)
+    compare(o, lse, o_ref, lse_ref, what=w.name)
+
+
+@pytest.fixture(scope="module")
+def inputs_8k():
+    return inputs.make_inputs(inputs.WORKLOADS["bf16_causal_8k"])
+
+
+@pytest.mark.parametrize("name", ["bf16_causal_8k", "bf16_noncausal_8k"])
+def test_8k_workloads_sampled(name, inputs_8k):
+    w = inputs.WORKLOADS[name]
+    x = inputs_8k
+    o, lse = run_gpu(x, causal=w.causal, softmax_scale=w.softmax_scale)
+    rows = sample_rows(w.batch, w.heads, w.seqlen_q, 256, seed=5)
+    o_ref, lse_ref = oracle.attention_rows(x["q"], x["k"], x["v"], rows,
+                                           softmax_scale=w.softmax_scale, causal=w.causal)
+    og, lg = gather_rows(o, lse, rows)
+    compare(og, lg, o_ref, lse_ref, what=name)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+
+
+def test_varlen_workload():
+    w = inputs.WORKLOADS["bf16_varlen_causal"]
+    x = inputs.make_inputs(w)
+    sq, sk = x["seqlens"]
+    cu_q = x["cu_seqlens_q"].numpy()
+    o, lse = run_gpu(x, causal=w.causal, softmax_scale=w.softmax_scale)
+    rows = sample_rows(len(sq), w.heads, None, 512, seed=6, seqlens_q=sq)
+    o_ref, lse_ref = oracle.attention_rows(x["q"], x["k"], x["v"], rows,
+                                           softmax_scale=w.softmax_scale, causal=w.causal,
+                                           cu_seqlens_q=x["cu_seqlens_q"],
+                                           cu_seqlens_k=x["cu_seqlens_k"])
+    og, lg = gather_rows(o, lse, rows, varlen=True, cu_q=cu_q)
+    compare(og, lg, o_ref, lse_ref, what=w.name)
+    # the sequences without keys: every row exactly O = 0, LSE = -inf
+    for b in w.empty_k_at:
+        assert sk[b] == 0 and sq[b] > 0
+        sl = slice(cu_q[b], cu_q[b + 1])
+        assert np.all(o[sl] == 0) and np.all(lse[:, sl] == -np.inf)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_small_full(causal):
+    sq = [5, 0, 130, 257, 1, 128, 40]
+    sk = [7, 3, 0, 300, 1, 128, 40]
+    x = inputs.make_varlen(sq, sk, heads=3, head_dim=128, seed=21)
+    o, lse = run_gpu(x, causal=causal, softmax_scale=128 ** -0.5)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=128 ** -0.5,
+                                      causal=causal, cu_seqlens_q=x["cu_seqlens_q"],
+                                      cu_seqlens_k=x["cu_seqlens_k"])
+    compare(o, lse, o_ref, lse_ref, what=f"varlen small causal={causal}")
+
+
+def test_fp8_small_full():
+    w = inputs.Workload("fp8_small", 2, 3, 300, 400, 128, False, dtype="e4m3", seed=31)
+    x = inputs.make_inputs(w)
+    for causal in (False, True):
+        o, lse = run_gpu(x, causal=causal, softmax_scale=w.softmax_scale)
+        o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=w.softmax_scale,
+                                          causal=causal, descale=x["descale"])
+        compare(o, lse, o_ref, lse_ref, dtype="e4m3", what=f"fp8 small causal={causal}")
+
+
+def test_fp8_workload_sampled():
+    w = inputs.WORKLOADS["fp8_noncausal_4k"]
+    x = inputs.make_inputs(w)
+    o, lse = run_gpu(x, causal=w.causal, softmax_scale=w.softmax_scale)
+    rows = sample_rows(w.batch, w.heads, w.seqlen_q, 256, seed=7)
+    o_ref, lse_ref = oracle.attention_rows(x["q"], x["k"], x["v"], rows,
+                                           softmax_scale=w.softmax_scale, causal=w.causal,
+                                           descale=x["descale"])
+    og, lg = gather_rows(o, lse, rows)
+    compare(og, lg, o_ref, lse_ref, dtype="e4m3", what=w.name)
+
+
+def test_shortq_longkv_split_and_unsplit():
+    w = inputs.WORKLOADS["bf16_shortq_longkv"]
+    x = inputs.make_inputs(w)
+    assert fa.num_splits(w.batch, w.heads, w.seqlen_q, w.seqlen_k) > 1
+    o_s, lse_s = run_gpu(x, causal=False, softmax_scale=w.softmax_scale, workspace="auto")
+    o_n, lse_n = run_gpu(x, causal=False, softmax_scale=w.softmax_scale, workspace=None)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=w.softmax_scale)
+    compare(o_s, lse_s, o_ref, lse_ref, what="short-q long-kv, split")
+    compare(o_n, lse_n, o_ref, lse_ref, what="short-q long-kv, unsplit")
+
+
+def test_split_causal_small():
+    # causal with a short query block against a long key range: splits whose
+    # key range lies beyond every row's diagonal produce -inf partials
+    x = inputs.make_random(1, 2, 200, 6000, 128, seed=41)
+    assert fa.num_splits(1, 2, 200, 6000, causal=True) > 1
+    o, lse = run_gpu(x, causal=True, softmax_scale=128 ** -0.5)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=128 ** -0.5,
+                                      causal=True)
+    compare(o, lse, o_ref, lse_ref, what="split causal")
+
+
+def test_zero_keys_fixed_length():
+    x = inputs.make_random(2, 2, 130, 0, 128, seed=3)
+    o, lse = run_gpu(x, causal=False, softmax_scale=0.1)
+    assert np.all(o == 0) and np.all(lse == -np.inf)
+
+
+def test_guard_bands_untouched():
+    B, H, S, D = 1, 2, 200, 128
+    x = to_dev(inputs.make_random(B, H, S, S, D, seed=8))
+    pad = 4096
+    o_buf = torch.full((2 * pad + B * S * H * D,), 7.0, dtype=torch.bfloat16, device="cuda")
+    l_buf = torch.full((2 * pad + B * H * S,), 9.0, dtype=torch.float32, device="cuda")
+    o = o_buf[pad:pad + B * S * H * D].view(B, S, H, D)
+    lse = l_buf[pad:pad + B * H * S].view(B, H, S)
+    fa.fwd(x["q"], x["k"], x["v"], causal=True, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(o_buf[:pad] == 7.0) and torch.all(o_buf[-pad:] == 7.0)
+    assert torch.all(l_buf[:pad] == 9.0) and torch.all(l_buf[-pad:] == 9.0)
+    assert torch.all(torch.isfinite(o))
+
+
+def test_rejected_call_writes_nothing():
+    x = to_dev(inputs.make_random(1, 1, 64, 64, 128, seed=9))
+    o = torch.full((1, 64, 1, 128), 3.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((1, 1, 64), 5.0, dtype=torch.float32, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.fwd(x["q"], x["k"], x["v"], softmax_scale=-1.0, out=o, lse=lse)
+    assert e.value.status == fa.FA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.all(o == 3.0) and torch.all(lse == 5.0)
+
+
+def test_deterministic():
+    x = to_dev(inputs.make_random(2, 4, 700, 900, 128, seed=10))
+    a = fa.fwd(x["q"], x["k"], x["v"], causal=True)
+    b = fa.fwd(x["q"], x["k"], x["v"], causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_bounded_wait_timeout_is_reported_and_context_survives():
+    x = to_dev(inputs.make_random(1, 2, 256, 256, 128, seed=11))
+    fa.device_error(clear=True)
+    fa.debug_set(wait_limit_ns=200_000_000, inject=1)  # withhold one Q-tile arrival
+    try:
+        fa.fwd(x["q"], x["k"], x["v"])
+        st, flags = fa.device_error(clear=True)
+    finally:
+        fa.debug_set(0, 0)
+    assert st == fa.FA_ERR_DEVICE_TIMEOUT
+    assert flags & 1 and (flags >> 8) & 0xFF == 3  # site: MMA issuer waiting for Q
+    # the context is still usable and results are right again
+    o, lse = fa.fwd(x["q"], x["k"], x["v"])
+    torch.cuda.synchronize()
+    assert fa.device_error(clear=True)[0] == fa.FA_OK
+    o_ref, lse_ref = oracle.attention(x["q"].cpu(), x["k"].cpu(), x["v"].cpu(),
+                                      softmax_scale=128 ** -0.5)
+    compare(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+            o_ref, lse_ref, what="after timeout")
