@@ -1,0 +1,414 @@
+"""Benchmark of the attention forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...     # the fp64 CPU oracle, timed on host cores
+
+Prints ONE JSON line (rank 0).  A step is one forward pass over the whole
+workload (default: bf16, causal, B=2 H=32 S=8192 D=128, inputs 2*N(0,1)):
+`value` is TFLOP/s with inputs resident in HBM, counted as 4*B*H*Sq*Sk*D
+(halved for causal), timed per step with CUDA events on the launching stream
+and the L2 flushed (a 256 MiB write) between timed steps; `e2e` is the same
+metric through the public API with pinned host inputs copied in and O/LSE
+copied out inside the timed region.  Under torchrun each rank runs the same
+workload on its own GPU (the pass shards over independent (batch, head)
+problems; no collective on the data path): value = all ranks' FLOPs / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOPS (bf16, causal, 8K, d=128) and % of GB300 tensor peak"
+DEFAULT_WORKLOAD = "bf16_causal_8k"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _flops(w, x) -> float:
+    """Algorithmic FLOPs of one pass: 4 * Sq * Sk * D per (batch, head), halved when causal."""
+    if w.varlen:
+        sq, sk = x["seqlens"]
+        tot = sum(4.0 * w.heads * a * b * w.head_dim for a, b in zip(sq, sk))
+    else:
+        tot = 4.0 * w.batch * w.heads * w.seqlen_q * w.seqlen_k * w.head_dim
+    return tot / 2 if w.causal else tot
+
+
+def _bytes(x) -> float:
+    """Compulsory HBM bytes of one pass: Q, K, V read once; O (bf16) and LSE (fp32) written."""
+    q, k, v = x["q"], x["k"], x["v"]
+    rows = q.numel() // q.shape[-1]  # query rows x heads = LSE entries
+    return (q.numel() + k.numel() + v.numel()) * q.element_size() + rows * v.shape[-1] * 2 + rows * 4
+
+
+def _source_sha() -> str:
+    """Hash of the kernel sources, to tell whether recorded ncu counters still apply."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_forward_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def _recorded_traffic(workload: str):
+    """DRAM bytes per launch of the forward kernel from a committed ncu summary, or None
+    if none was recorded for this workload or the kernel sources changed since."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_sha") != _source_sha():
+        return None
+    return rec.get("bytes_per_launch")
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        import torch
+        args = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                "-lms", "100"]
+        try:
+            prop = torch.cuda.get_device_properties(self.dev)
+            bus = f"{prop.pci_domain_id:08X}:{prop.pci_bus_id:02X}:{prop.pci_device_id:02X}.0"
+            args += ["-i", bus]
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(args, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline)
+def _oracle_rows_flops(w, rows):
+    sq, sk = w.seqlen_q, w.seqlen_k
+    tot = 0.0
+    for _, _, i in rows:
+        n = sk if not w.causal else max(0, min(sk, i + sk - sq + 1))
+        tot += 4.0 * n * w.head_dim
+    return tot
+
+
+def _oracle_sample(w, x, budget_s: float, seed: int = 0):
+    """Time the oracle on seeded random rows of the workload until ~budget_s of CPU work."""
+    import numpy as np
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    n = 16
+    while True:
+        rows = np.stack([rng.integers(0, w.batch, n), rng.integers(0, w.heads, n),
+                         rng.integers(0, w.seqlen_q, n)], axis=1).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.attention_rows(x["q"], x["k"], x["v"], rows, softmax_scale=w.softmax_scale,
+                              causal=w.causal, descale=x["descale"])
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or n >= w.batch * w.heads * w.seqlen_q:
+            return _oracle_rows_flops(w, rows), dt, n
+        grow = max(2.0, min(16.0, budget_s / max(dt, 1e-3)))
+        n = int(n * grow)
+
+
+def _oracle_threads():
+    n = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return int(os.environ.get("OMP_NUM_THREADS", n))
+
+
+def run_reference(args, w):
+    """The reference arm: the fp64 oracle, as it stands, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    os.environ.setdefault("OMP_NUM_THREADS", str(_oracle_threads()))
+    from exact_attention_forward_gb300 import inputs
+    x = inputs.make_inputs(w)
+    per_step = max(2.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        _oracle_sample(w, x, per_step / 4, seed=1)
+    flops = secs = 0.0
+    rows_total = 0
+    for s in range(args.steps):
+        f, dt, n = _oracle_sample(w, x, per_step, seed=100 + s)
+        flops += f
+        secs += dt
+        rows_total += n
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w, "n/a (CPU)"),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _oracle_threads(),
+                         "kind": "oracle",
+                         "sample": f"{rows_total} seeded random query rows of {w.name} "
+                                   f"over {args.steps} steps"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(w, l2):
+    c = {"workload": w.name, "batch": w.batch, "heads": w.heads, "seqlen_q": w.seqlen_q,
+         "seqlen_k": w.seqlen_k, "head_dim": w.head_dim, "causal": w.causal,
+         "input_dtype": w.dtype, "values": f"{w.amp:g}*N(0,1) seed {w.seed}", "l2": l2}
+    if w.varlen:
+        c["varlen"] = f"{w.n_seqs} seqs U{{1..{w.seqlen_q}}} + {len(w.empty_k_at)} with Sk=0"
+    return c
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_forward_gb300 as fa
+    from exact_attention_forward_gb300 import inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    fa.load_library()
+
+    x = inputs.make_inputs(w)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    cu_q = x["cu_seqlens_q"].to(dev) if w.varlen else None
+    cu_k = x["cu_seqlens_k"].to(dev) if w.varlen else None
+    fp8 = w.dtype == "e4m3"
+    descale = [torch.tensor(d, dtype=torch.float32, device=dev) for d in x["descale"]] if fp8 else None
+    o_shape = (q.shape[0], q.shape[1], q.shape[2], v.shape[-1]) if not w.varlen else \
+        (q.shape[0], q.shape[1], v.shape[-1])
+    o = torch.empty(o_shape, dtype=torch.bfloat16, device=dev)
+    lse_shape = (w.batch, w.heads, w.seqlen_q) if not w.varlen else (w.heads, q.shape[0])
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    ws = None
+    if not w.varlen:
+        need = fa.workspace_size(w.batch, w.heads, w.seqlen_q, w.seqlen_k, w.head_dim, w.causal)
+        if need:
+            ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    splits = fa.num_splits(w.batch, w.heads, w.seqlen_q, w.seqlen_k, w.causal) if ws is not None else 1
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fwd(q, k, v, causal=w.causal, softmax_scale=w.softmax_scale, cu_seqlens_q=cu_q,
+               cu_seqlens_k=cu_k, max_seqlen_q=x["max_seqlen_q"], max_seqlen_k=x["max_seqlen_k"],
+               descale=descale, workspace=ws, out=o, lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st, flags = fa.device_error(clear=True)
+    if st != 0:
+        raise RuntimeError(f"device error word {flags:#x} after warm-up")
+
+    sampler = ClockSampler(dev.index)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.zero_()  # evict the previous step's working set from L2 (not timed)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(times_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flops = _flops(w, x)
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    ms_per_step = total_ms / args.steps
+
+    # ---------------- end to end through the public API, host buffers
+    e2e = None
+    if not args.skip_e2e:
+        hq, hk, hv = (t.cpu().pin_memory() for t in (x["q"], x["k"], x["v"]))
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        dq, dk, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv_.copy_(hv, non_blocking=True)
+            oo, ll = fa.fwd(dq, dk, dv_, causal=w.causal, softmax_scale=w.softmax_scale,
+                            cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=x["max_seqlen_q"],
+                            max_seqlen_k=x["max_seqlen_k"], descale=descale, workspace=ws,
+                            out=o, lse=lse, stream=stream)
+            ho.copy_(oo, non_blocking=True)
+            hl.copy_(ll, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(3, min(args.steps, 20))
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        e2e = {"value": world * flops * n_e2e / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_ms / n_e2e}
+
+    st, flags = fa.device_error(clear=True)
+    if st != 0:
+        raise RuntimeError(f"device error word {flags:#x} after timing")
+
+    peaks, peak_src = _peaks()
+    kernel_ms = ms_per_step
+    if w.seqlen_q <= 256 and not w.varlen and not w.causal and splits > 1:
+        bound, unit = "hbm", "GB/s"
+        achieved = _bytes(x) / (kernel_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+    else:
+        bound, unit = "tensor", "TFLOP/s"
+        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": _recorded_traffic(w.name),
+                "peak_source": f"{peak_src} MEASURED_PEAKS.json burst"
+                               + (" x2 (fp8/bf16 nominal ratio)" if fp8 and bound == "tensor" else ""),
+                "frac_of_sustained": (achieved / (peaks.get("bf16_tflops_sustained", peak)
+                                                  * (2.0 if fp8 else 1.0))
+                                      if bound == "tensor" else None)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if not fp8 else "e4m3", "data": "synthetic",
+        "config": _config(w, "flushed between timed steps (256 MiB write)"),
+        "clocks": clocks, "e2e": e2e,
+        "gpu_launches": args.steps * (2 if splits > 1 else 1),
+        "roofline": roofline,
+        "step_ms": {"min": min(times_ms), "median": statistics.median(times_ms),
+                    "max": max(times_ms)},
+        "key_splits": splits,
+    }
+    if rank == 0 and not args.skip_cpu_baseline and world == 1:
+        os.environ.setdefault("OMP_NUM_THREADS", str(_oracle_threads()))
+        f, dt, n = _oracle_sample(w, x, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": f / dt / 1e12, "unit": "TFLOP/s",
+                                "cores": _oracle_threads(), "kind": "oracle",
+                                "sample": f"{n} seeded random query rows of {w.name} "
+                                          f"({dt:.1f} s, fp64)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    from exact_attention_forward_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

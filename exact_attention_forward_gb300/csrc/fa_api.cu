@@ -233,7 +233,10 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  void* workspace, size_t workspace_bytes, void* stream) {
     t_detail[0] = '\0';
     // ---------------------------------------------------------------- validation
-    if (!q || !k || !v || !o || !lse)
+    const bool varlen = cu_seqlens_q != nullptr || cu_seqlens_k != nullptr;
+    // with no key rows at all (fixed length seqlen_k == 0, or varlen total 0) K and V may be NULL
+    const bool no_keys = seqlen_k == 0;
+    if (!q || !o || !lse || (!no_keys && (!k || !v)))
         return fail(FA_ERR_INVALID_ARG, "q, k, v, o and lse must be non-NULL device pointers");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return fail(FA_ERR_INVALID_ARG, "q, k, v, o and lse must be 16-byte aligned");
@@ -250,7 +253,6 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
         (k_descale && (reinterpret_cast<uintptr_t>(k_descale) & 3u)) ||
         (v_descale && (reinterpret_cast<uintptr_t>(v_descale) & 3u)))
         return fail(FA_ERR_INVALID_ARG, "descale pointers must be 4-byte aligned");
-    const bool varlen = cu_seqlens_q != nullptr || cu_seqlens_k != nullptr;
     if (varlen && (!cu_seqlens_q || !cu_seqlens_k))
         return fail(FA_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k must both be given");
     if (varlen && (max_seqlen_q < 0 || max_seqlen_k < 0))
@@ -329,8 +331,13 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     // fixed length: (d, head, seq row, batch); varlen: (d, head, packed row, 1)
     const int nbat = varlen ? 1 : batch;
     if ((st = encode_map(&tq, q, fp8, head_dim, heads, seqlen_q, nbat)) != FA_OK) return st;
-    if ((st = encode_map(&tk, k, fp8, head_dim, heads, seqlen_k, nbat)) != FA_OK) return st;
-    if ((st = encode_map(&tv, v, fp8, head_dim, heads, seqlen_k, nbat)) != FA_OK) return st;
+    if (no_keys) {  // no key block is ever loaded; any valid map will do
+        tk = tq;
+        tv = tq;
+    } else {
+        if ((st = encode_map(&tk, k, fp8, head_dim, heads, seqlen_k, nbat)) != FA_OK) return st;
+        if ((st = encode_map(&tv, v, fp8, head_dim, heads, seqlen_k, nbat)) != FA_OK) return st;
+    }
 
     // ---------------------------------------------------------------- launch
     const int grid = (int)(n_items < sms ? n_items : sms);

@@ -162,13 +162,13 @@ struct WaitCtx {
 };
 
 static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
-                                       uint32_t site) {
+                                                 uint32_t site, bool honor_abort = true) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 128; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (*w.abort_flag) return false;
+        if (honor_abort && *w.abort_flag) return false;
         if (globaltimer_ns() - t0 > w.limit_ns) {
             atomicCAS(w.err, 0u, kErrTimeout | (site << 8));
             atomicOr(w.err, kErrTimeout);
@@ -429,9 +429,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++o_cnt[t];
                 }
             }
-            // Drain: every MMA issued by this thread has completed before TMEM is released.
+            // Drain: every MMA issued by this thread has completed before TMEM is
+            // released, also after an abort (bounded by the wait limit only).
             umma_commit(bar(C::DRAIN));
-            wait_bar(bar(C::DRAIN), 0u, wc, SITE_DRAIN);
+            if (!mbar_try_wait(bar(C::DRAIN), 0u)) wait_slow(bar(C::DRAIN), 0u, wc, SITE_DRAIN, false);
         }
         __syncwarp();
     }
@@ -535,11 +536,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mx3 = fmaxf(mx3, s[c + 3]);
                 }
                 const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
-                if (m_cand > m_run + kTau) {
-                    // the reference max grows: rescale l and (except on the first block,
-                    // whose PV overwrites O) the accumulated O of this row.
-                    const float f = ex2_approx(m_run - m_cand);  // 0 when m_run = -inf
-                    if (j != j_first && m_run != -INFINITY) {
+                // Lazy rescale: the reference max moves only when it grows by more than
+                // 2^kTau.  tcgen05.ld/st are warp-collective (.sync.aligned), so the O
+                // round trip is taken by the whole warp whenever any of its rows needs it;
+                // rows that keep their reference scale by 1.
+                const bool grow = m_cand > m_run + kTau;
+                if (__any_sync(0xffffffffu, grow)) {
+                    const float f = grow ? ex2_approx(m_run - m_cand) : 1.0f;  // 0 if m_run = -inf
+                    if (j != j_first) {  // the first block's PV overwrites O (uniform per warp)
 #pragma unroll 1
                         for (int c = 0; c < D; c += 16) {
                             uint32_t orr[16];
@@ -551,8 +555,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tmem_st16(t_o + c, orr);
                         }
                     }
-                    l_run *= f;
-                    m_run = m_cand;
+                    if (grow) {
+                        l_run *= f;
+                        m_run = m_cand;
+                    }
                 }
                 const float mu = (m_run == -INFINITY) ? 0.0f : m_run;
                 float ls0 = 0.f, ls1 = 0.f;
@@ -635,6 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     __syncthreads();
     if (warp == 1) {
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }

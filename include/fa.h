@@ -23,8 +23,9 @@
  *
  * Conventions for every entry point:
  *  - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
- *    aligned.  The library allocates no device memory, never synchronises the
- *    stream, and keeps only host-side caches.
+ *    aligned (k and v may be NULL when seqlen_k == 0: no key rows exist).
+ *    The library allocates no device memory, never synchronises the stream,
+ *    and keeps only host-side caches.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
  *  - Every argument is validated before anything is launched; on a non-OK
  *    status nothing has been written and fa_last_error_detail() says why.
