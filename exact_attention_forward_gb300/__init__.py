@@ -32,7 +32,8 @@ FA_DTYPE_BF16, FA_DTYPE_E4M3 = 0, 1
 
 # Every function declared in include/fa.h.
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_num_splits", "fa_status_string",
-                    "fa_last_error_detail", "fa_device_error", "fa_debug_set")
+                    "fa_last_error_detail", "fa_device_error", "fa_debug_set",
+                    "fa_fwd_static_workspace")
 
 _lock = threading.Lock()
 _lib = None
@@ -76,6 +77,9 @@ def load_library():
         lib.fa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         lib.fa_debug_set.restype = None
         lib.fa_debug_set.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
+        lib.fa_fwd_static_workspace.restype = i32
+        lib.fa_fwd_static_workspace.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                                f32, i32, i32, vp, vp, vp, vp]
         _lib = lib
         return lib
 

@@ -105,6 +105,33 @@ size_t fa_fwd_workspace_size(int batch, int heads, int seqlen_q, int seqlen_k,
 /* Number of key splits fa_fwd would use for that shape with a workspace. */
 int fa_fwd_num_splits(int batch, int heads, int seqlen_q, int seqlen_k, int causal);
 
+/*
+ * fa_fwd_static_workspace -- fa_fwd for fixed-length inputs, for callers that
+ * cannot allocate device memory: code embedded in a host program that owns
+ * all device memory and gives out no scratch (plugins, for instance), or
+ * latency-critical loops where cudaMalloc/cudaFree would synchronise the
+ * device.  The paper has no counterpart: this is a packaging of the split
+ * path above, not a step of the method.
+ *
+ * Arguments are those of fa_fwd without cu_seqlens and without workspace.
+ * When the shape splits its key range, the partial results go to a 16 MiB
+ * array that the library holds in device memory (reserved on every GPU that
+ * loads the library, until the process exits).  Shapes needing more return
+ * FA_ERR_WORKSPACE and launch nothing.  All calls on a device share that
+ * array: calls whose kernels overlap on the GPU race and corrupt each other;
+ * nothing in it needs to start at zero.  The first call on a device looks up
+ * the array's device address, so make it before any stream capture.  This
+ * entry point itself allocates nothing.
+ */
+fa_status fa_fwd_static_workspace(const void* q, const void* k, const void* v,
+                                  void* o, float* lse,
+                                  int batch, int heads, int seqlen_q, int seqlen_k,
+                                  int head_dim, int head_dim_v, float softmax_scale, int causal,
+                                  fa_dtype dtype,
+                                  const float* q_descale, const float* k_descale,
+                                  const float* v_descale,
+                                  void* stream);
+
 /* Static description of a status code. */
 const char* fa_status_string(fa_status status);
 
