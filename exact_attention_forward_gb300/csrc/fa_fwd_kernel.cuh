@@ -40,28 +40,58 @@
 //     order, so S_t(j-1) overwriting P_t(j) after PV_t(j) is safe, and S_t(j)
 //     being complete implies PV_t(j+1) is complete -- which is what lets the
 //     softmax warps rescale O_t in place (lazily, only when the running max
-//     grows by more than 2^8) without a separate correction warpgroup;
+//     grows by more than 2^16 for bf16 P, 2^8 for e4m3 P) without a separate
+//     correction warpgroup;
+//   * the MMA issuer is one thread whose bookkeeping between MMA batches is kept
+//     minimal (compile-time tile indices, phase bits in registers, descriptors
+//     built once): measured, a second issuer thread per tile interleaving MMA
+//     streams is slower, and so is moving part of exp2 to the FMA pipe -- on
+//     GB300 the MUFU is not the limit;
 //   * every wait is bounded by wall clock; a timeout sets the device error
 //     word and all roles abandon the launch cleanly (TMEM released).
 #pragma once
 
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
 namespace fa {
-
 constexpr int kBM = 128;          // query rows per tile (one TMEM lane per row)
 constexpr int kBN = 128;          // keys per K/V block
 constexpr int kTiles = 2;         // query tiles per work item
 constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kTau = 8.0f;      // lazy-rescale threshold (log2 units): p <= 2^8
+// Pairs (of every 16) of exp2 evaluated on the FMA pipe instead of the MUFU, in
+// blocks without masking.  0 by default: on GB300 the MUFU keeps up (measured), and
+// the extra instructions only lengthen the softmax; kept as a build option.
+#ifndef FA_EXP2_EMU_PAIRS
+#define FA_EXP2_EMU_PAIRS 0
+#endif
+// Lazy-rescale threshold (log2 units): P stays <= 2^tau.  e4m3 P must stay below its
+// 448 maximum; bf16 P has fp32's exponent range, so a larger threshold only trades
+// (rare) rescales for larger -- still exactly representable -- P values.
+template <bool FP8>
+__host__ __device__ constexpr float lazy_tau() { return FP8 ? 8.0f : 16.0f; }
+
+// exp2 on the FMA pipe (for part of the columns, relieving the MUFU): Cody-Waite
+// style range reduction x = n + f with n = round(x), |f| <= 1/2, then 2^f by a
+// degree-3 polynomial, minimax in relative error on [-1/2, 1/2] (coefficients
+// derived by linear programming in exact_attention_forward_gb300/exp2_poly.py;
+// max relative error 7.5e-5, below bf16's 2^-9 rounding of P), and 2^n added to
+// the exponent field.  Inputs are clamped to >= -125 so the result stays normal.
+constexpr float kExp2C0 = 0.9999279975891113f;
+constexpr float kExp2C1 = 0.6932609677314758f;
+constexpr float kExp2C2 = 0.2426113784313202f;
+constexpr float kExp2C3 = 0.05517187342047691f;
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + magic rounds x to an integer
+
 // Register split: launched at 168 per thread (384 x 168 = 64512); the producer /
-// MMA warpgroup gives up 48 per thread, the two softmax warpgroups take 24 more.
-constexpr uint32_t kRegsLoadMma = 120;
-constexpr uint32_t kRegsSoftmax = 192;
+// MMA warpgroup gives up 64 per thread, the two softmax warpgroups take 32 more.
+constexpr uint32_t kRegsLoadMma = 104;
+constexpr uint32_t kRegsSoftmax = 200;
 static_assert(128 * kRegsLoadMma + 256 * kRegsSoftmax <= 384 * 168, "register split exceeds launch");
 
 template <int D, bool FP8>
@@ -214,9 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::Q_FULL + t), 1);
             mbar_init(bar(C::Q_EMPTY + t), 1);
             mbar_init(bar(C::S_FULL + t), 1);
-            mbar_init(bar(C::P_FULL + t), kBM);
+            mbar_init(bar(C::P_FULL + t), kBM / 32);   // one arrival per softmax warp
             mbar_init(bar(C::O_FULL + t), 1);
-            mbar_init(bar(C::O_EMPTY + t), kBM);
+            mbar_init(bar(C::O_EMPTY + t), kBM / 32);
         }
         mbar_init(bar(C::DRAIN), 1);
         for (int s = 0; s < C::kStages; ++s) {
@@ -248,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tm_v);
             const uint64_t pol_q = l2_policy_evict_first();
             const uint64_t pol_kv = l2_policy_evict_last();
-            uint32_t ring = 0, q_cnt[kTiles] = {0, 0};
+            uint32_t ring = 0, ph_qe = 0;  // bit t: parity of the last Q_EMPTY wait of tile t
             bool withheld = false;
             bool aborted = false;
             for (int round = 0; !aborted; ++round) {
@@ -256,29 +286,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (w >= p.n_items) break;
                 const Item it = decode_item(p, w);
                 if (it.n_hi <= it.n_lo) continue;
-                const int qb = p.varlen ? 0 : it.b;
-                const int kb = qb;
-                for (int t = 0; t < kTiles && !aborted; ++t) {
-                    if (it.n_hi_t[t] <= it.n_lo) continue;
-                    if (!wait_bar(bar(C::Q_EMPTY + t), (q_cnt[t] & 1u) ^ 1u, wc, SITE_Q_EMPTY)) {
-                        aborted = true;
-                        break;
-                    }
-                    ++q_cnt[t];
+                const int bc = p.varlen ? 0 : it.b;  // batch coordinate of the 4-D view
+                auto load_q = [&](auto tc) -> bool {
+                    constexpr int t = decltype(tc)::value;
+                    if (it.n_hi_t[t] <= it.n_lo) return true;
+                    if (!wait_bar(bar(C::Q_EMPTY + t), ((ph_qe >> t) & 1u) ^ 1u, wc, SITE_Q_EMPTY))
+                        return false;
+                    ph_qe ^= 1u << t;
                     if (p.inject == 1u && !withheld) {  // debug: never arrive on this Q tile
                         withheld = true;
-                        continue;
+                        return true;
                     }
                     const int qrow = (p.varlen ? it.q_row0 : 0) + it.m0[t];
                     mbar_arrive_expect_tx(bar(C::Q_FULL + t), C::kTileBytes);
 #pragma unroll
                     for (int c = 0; c < C::kChunks; ++c)
                         tma_load_4d(s_q + t * C::kTileBytes + c * C::kChunkBytes, &tm_q,
-                                    bar(C::Q_FULL + t), c * C::kChunkElems, it.h, qrow, qb, pol_q);
+                                    bar(C::Q_FULL + t), c * C::kChunkElems, it.h, qrow, bc, pol_q);
+                    return true;
+                };
+                if (!load_q(std::integral_constant<int, 0>{}) || !load_q(std::integral_constant<int, 1>{})) {
+                    aborted = true;
+                    break;
                 }
                 for (int j = it.n_hi - 1; j >= it.n_lo && !aborted; --j) {
                     const int krow = (p.varlen ? it.k_row0 : 0) + j * kBN;
-#pragma unroll 1
+#pragma unroll
                     for (int kv = 0; kv < 2; ++kv) {
                         const uint32_t slot = ring % C::kStages;
                         const uint32_t ph = (ring / C::kStages) & 1u;
@@ -291,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int c = 0; c < C::kChunks; ++c)
                             tma_load_4d(s_kv + slot * C::kTileBytes + c * C::kChunkBytes,
                                         kv ? &tm_v : &tm_k, bar(C::KV_FULL + slot),
-                                        c * C::kChunkElems, it.h, krow, kb, pol_kv);
+                                        c * C::kChunkElems, it.h, krow, bc, pol_kv);
                         ++ring;
                     }
                 }
@@ -305,40 +338,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // One thread issues every MMA.  Its bookkeeping sits between MMA batches, so
+        // it is kept lean: tiles are unrolled at compile time (phase bits live in
+        // registers), and descriptors are built once -- per MMA only the 32-bit low
+        // word (start address) advances.
         if (lane == 0) {
-            uint32_t ring = 0, q_cnt[kTiles] = {0, 0}, p_cnt[kTiles] = {0, 0},
-                     o_cnt[kTiles] = {0, 0};
+            // descriptor words: high word (SBO = 1024 B, version 1, 128B swizzle) is common
+            const uint32_t d_hi = (uint32_t)(sdesc_sw128(0, 16, 1024) >> 32);
+            const uint32_t q_lo = (uint32_t)sdesc_sw128(s_q, 16, 1024);          // + t*tile
+            const uint32_t k_lo = (uint32_t)sdesc_sw128(s_kv, 16, 1024);         // + slot*tile
+            const uint32_t v_lo = (uint32_t)sdesc_sw128(s_kv, C::kChunkBytes, 1024);
+            constexpr uint32_t kTile16 = C::kTileBytes >> 4;
+            auto desc = [&](uint32_t lo) -> uint64_t { return ((uint64_t)d_hi << 32) | lo; };
+            uint32_t ring = 0;
+            uint32_t ph_q = 0, ph_p = 0, ph_o = 0;  // bit t: parity of the next wait on tile t
             bool aborted = false;
             // S_t = Q_t K^T : A = Q (K-major), B = K (K-major), both 128B-swizzled.
-            auto issue_qk = [&](int t, uint32_t kslot) {
-                const uint32_t q_addr = s_q + t * C::kTileBytes;
-                const uint32_t k_addr = s_kv + kslot * C::kTileBytes;
+            auto issue_qk = [&](auto tc, uint32_t kslot) {
+                constexpr int t = decltype(tc)::value;
+                const uint32_t a0 = q_lo + t * kTile16, b0 = k_lo + kslot * kTile16;
 #pragma unroll
                 for (int kk = 0; kk < D / C::kUmmaK; ++kk) {
-                    const int c = kk * C::kUmmaK / C::kChunkElems;
-                    const int sub = (kk * 32) % 128;  // byte offset inside the 128-byte atom row
-                    const uint64_t a = sdesc_sw128(q_addr + c * C::kChunkBytes + sub, 16, 1024);
-                    const uint64_t b = sdesc_sw128(k_addr + c * C::kChunkBytes + sub, 16, 1024);
+                    // k step kk: 32 bytes further along the row, next 128-byte atom column
+                    constexpr uint32_t kAtom = C::kChunkBytes >> 4;
+                    const uint32_t off = (uint32_t)((kk * C::kUmmaK) / C::kChunkElems) * kAtom +
+                                         (uint32_t)((kk * 32) % 128 >> 4);
                     if constexpr (FP8)
-                        umma_f8_ss(tmem_base + 128u * t, a, b, C::kIdescQK, kk > 0);
+                        umma_f8_ss(tmem_base + 128u * t, desc(a0 + off), desc(b0 + off), C::kIdescQK, kk > 0);
                     else
-                        umma_f16_ss(tmem_base + 128u * t, a, b, C::kIdescQK, kk > 0);
+                        umma_f16_ss(tmem_base + 128u * t, desc(a0 + off), desc(b0 + off), C::kIdescQK, kk > 0);
                 }
             };
             // O_t += P_t V : A = P_t from TMEM, B = V (MN-major, 128B-swizzled):
             // leading offset = next 128-byte column atom, stride offset = next 8 keys.
-            auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
-                const uint32_t v_addr = s_kv + vslot * C::kTileBytes;
+            auto issue_pv = [&](auto tc, uint32_t vslot, uint32_t acc) {
+                constexpr int t = decltype(tc)::value;
+                const uint32_t b0 = v_lo + vslot * kTile16;
 #pragma unroll
                 for (int kk = 0; kk < kBN / C::kUmmaK; ++kk) {
-                    const uint64_t b = sdesc_sw128(v_addr + kk * C::kUmmaK * 128, C::kChunkBytes, 1024);
+                    const uint32_t off = (uint32_t)(kk * C::kUmmaK * 128) >> 4;
                     const uint32_t a_tmem = tmem_base + 128u * t + 8u * kk;
                     if constexpr (FP8)
-                        umma_f8_ts(tmem_base + C::kColO + 128u * t, a_tmem, b, C::kIdescPV,
-                                   (acc || kk > 0) ? 1u : 0u);
+                        umma_f8_ts(tmem_base + C::kColO + 128u * t, a_tmem, desc(b0 + off), C::kIdescPV,
+                                   kk > 0 ? 1u : acc);
                     else
-                        umma_f16_ts(tmem_base + C::kColO + 128u * t, a_tmem, b, C::kIdescPV,
-                                    (acc || kk > 0) ? 1u : 0u);
+                        umma_f16_ts(tmem_base + C::kColO + 128u * t, a_tmem, desc(b0 + off), C::kIdescPV,
+                                    kk > 0 ? 1u : acc);
                 }
             };
             for (int round = 0; !aborted; ++round) {
@@ -346,88 +391,78 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (w >= p.n_items) break;
                 const Item it = decode_item(p, w);
                 if (it.n_hi <= it.n_lo) continue;
-                for (int t = 0; t < kTiles; ++t) {
-                    if (it.n_hi_t[t] <= it.n_lo) continue;
-                    if (!wait_bar(bar(C::Q_FULL + t), q_cnt[t] & 1u, wc, SITE_Q_FULL)) {
-                        aborted = true;
-                        break;
-                    }
-                }
-                if (aborted) break;
+                const int hi0 = it.n_hi_t[0], hi1 = it.n_hi_t[1], lo = it.n_lo;
+                const bool has0 = hi0 > lo, has1 = hi1 > lo;
+                if (has0 && !wait_bar(bar(C::Q_FULL + 0), ph_q & 1u, wc, SITE_Q_FULL)) break;
+                if (has1 && !wait_bar(bar(C::Q_FULL + 1), (ph_q >> 1) & 1u, wc, SITE_Q_FULL)) break;
                 tc_fence_after();
-                bool first[kTiles] = {true, true};
+                uint32_t acc0 = 0u, acc1 = 0u;  // becomes 1 after the tile's first PV
                 const int j0 = it.n_hi - 1;
-                uint32_t kslot = ring % C::kStages;
-                if (!wait_bar(bar(C::KV_FULL + kslot), (ring / C::kStages) & 1u, wc, SITE_KV_FULL)) {
-                    aborted = true;
+                const uint32_t kslot0 = ring % C::kStages;
+                if (!wait_bar(bar(C::KV_FULL + kslot0), (ring / C::kStages) & 1u, wc, SITE_KV_FULL))
                     break;
-                }
                 ++ring;
-                for (int t = 0; t < kTiles; ++t) {
-                    if (j0 < it.n_hi_t[t]) {
-                        issue_qk(t, kslot);
-                        umma_commit(bar(C::S_FULL + t));
-                    }
+                if (j0 < hi0) {
+                    issue_qk(std::integral_constant<int, 0>{}, kslot0);
+                    umma_commit(bar(C::S_FULL + 0));
                 }
-                umma_commit(bar(C::KV_EMPTY + kslot));
-                for (int j = j0; j >= it.n_lo && !aborted; --j) {
+                if (j0 < hi1) {
+                    issue_qk(std::integral_constant<int, 1>{}, kslot0);
+                    umma_commit(bar(C::S_FULL + 1));
+                }
+                umma_commit(bar(C::KV_EMPTY + kslot0));
+                for (int j = j0; j >= lo; --j) {
                     const uint32_t vslot = ring % C::kStages;
                     if (!wait_bar(bar(C::KV_FULL + vslot), (ring / C::kStages) & 1u, wc, SITE_KV_FULL)) {
                         aborted = true;
                         break;
                     }
                     ++ring;
-                    const bool has_next = j - 1 >= it.n_lo;
-                    uint32_t nslot = 0, nph = 0;
+                    const bool has_next = j - 1 >= lo;
+                    const uint32_t nslot = ring % C::kStages;
+                    const uint32_t nph = (ring / C::kStages) & 1u;
+                    if (has_next) ++ring;
                     bool next_ready = false;
-                    if (has_next) {
-                        nslot = ring % C::kStages;
-                        nph = (ring / C::kStages) & 1u;
-                        ++ring;
-                    }
-                    for (int t = 0; t < kTiles; ++t) {
-                        const bool cur = j < it.n_hi_t[t];
-                        const bool nxt = has_next && (j - 1) < it.n_hi_t[t];
+                    // one tile: PV_t(j) if it visits block j, then S_t(j-1) if it visits j-1
+                    auto tile_step = [&](auto tc, int hi, uint32_t& acc) -> bool {
+                        constexpr int t = decltype(tc)::value;
+                        const bool cur = j < hi;
+                        const bool nxt = has_next && (j - 1) < hi;
                         if (cur) {
-                            if (!wait_bar(bar(C::P_FULL + t), p_cnt[t] & 1u, wc, SITE_P_FULL)) {
-                                aborted = true;
-                                break;
-                            }
-                            ++p_cnt[t];
-                            if (first[t] &&
-                                !wait_bar(bar(C::O_EMPTY + t), (o_cnt[t] & 1u) ^ 1u, wc, SITE_O_EMPTY)) {
-                                aborted = true;
-                                break;
-                            }
+                            if (!wait_bar(bar(C::P_FULL + t), (ph_p >> t) & 1u, wc, SITE_P_FULL)) return false;
+                            ph_p ^= 1u << t;
+                            if (acc == 0u &&
+                                !wait_bar(bar(C::O_EMPTY + t), ((ph_o >> t) & 1u) ^ 1u, wc, SITE_O_EMPTY))
+                                return false;
                             tc_fence_after();
-                            issue_pv(t, vslot, !first[t]);
-                            first[t] = false;
+                            issue_pv(tc, vslot, acc);
+                            acc = 1u;
                         }
                         if (nxt) {
                             if (!next_ready) {
-                                if (!wait_bar(bar(C::KV_FULL + nslot), nph, wc, SITE_KV_FULL)) {
-                                    aborted = true;
-                                    break;
-                                }
+                                if (!wait_bar(bar(C::KV_FULL + nslot), nph, wc, SITE_KV_FULL)) return false;
                                 next_ready = true;
                             }
-                            issue_qk(t, nslot);
+                            issue_qk(tc, nslot);
                             umma_commit(bar(C::S_FULL + t));
                         } else if (cur) {
                             umma_commit(bar(C::O_FULL + t));  // last block of tile t
                         }
+                        return true;
+                    };
+                    if (!tile_step(std::integral_constant<int, 0>{}, hi0, acc0) ||
+                        !tile_step(std::integral_constant<int, 1>{}, hi1, acc1)) {
+                        aborted = true;
+                        break;
                     }
-                    if (aborted) break;
                     umma_commit(bar(C::KV_EMPTY + vslot));
                     if (has_next) umma_commit(bar(C::KV_EMPTY + nslot));
                 }
                 if (aborted) break;
-                for (int t = 0; t < kTiles; ++t) {
-                    if (it.n_hi_t[t] <= it.n_lo) continue;
-                    umma_commit(bar(C::Q_EMPTY + t));
-                    ++q_cnt[t];
-                    ++o_cnt[t];
-                }
+                if (has0) umma_commit(bar(C::Q_EMPTY + 0));
+                if (has1) umma_commit(bar(C::Q_EMPTY + 1));
+                ph_q ^= (has0 ? 1u : 0u) | (has1 ? 2u : 0u);
+                ph_o ^= (has0 ? 1u : 0u) | (has1 ? 2u : 0u);
             }
             // Drain: every MMA issued by this thread has completed before TMEM is
             // released, also after an abort (bounded by the wait limit only).
@@ -459,8 +494,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int w = item_of_round(round, nctas);
             if (w >= p.n_items) break;
             const Item it = decode_item(p, w);
-            if (!it.active[t]) continue;
-            const int row = it.m0[t] + r_in_tile;  // row within the sequence
+            // this warpgroup's tile, selected without indexing (keeps Item in registers)
+            const bool t_active = t ? it.active[1] : it.active[0];
+            const int t_m0 = t ? it.m0[1] : it.m0[0];
+            const int t_hi = t ? it.n_hi_t[1] : it.n_hi_t[0];
+            if (!t_active) continue;
+            const int row = t_m0 + r_in_tile;  // row within the sequence
             const bool row_ok = row < it.sq;
             // output addresses
             float* lse_ptr;
@@ -480,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 o_ptr = reinterpret_cast<__nv_bfloat16*>(p.o) +
                         (((size_t)it.b * p.seqlen_q + row) * p.heads + it.h) * D;
             }
-            if (it.n_hi_t[t] <= it.n_lo) {
+            if (t_hi <= it.n_lo) {
                 // no visible key for any row of this tile: O = 0, LSE = -inf
                 if (row_ok) {
                     if (p.split) {
@@ -497,11 +536,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // visible keys of this row: [0, vis_end) with vis_end = min(sk, row + sk - sq + 1)
             const int vis_end = p.causal ? min(it.sk, row + it.sk - it.sq + 1) : it.sk;
             // a block needs masking iff some column of it is invisible to some row of the tile
-            const int tile_rmin = it.m0[t];
+            const int tile_rmin = t_m0;
             const int tile_vis_min = p.causal ? min(it.sk, tile_rmin + it.sk - it.sq + 1) : it.sk;
             float m_run = -INFINITY;  // running max of scale_log2 * s (lazy reference)
             float l_run = 0.0f;       // running sum of exp2(scale_log2 * s - m_run)
-            const int j_first = it.n_hi_t[t] - 1;
+            const int j_first = t_hi - 1;
             for (int j = j_first; j >= it.n_lo; --j) {
                 bool ok = wait_bar(bar(C::S_FULL + t), s_cnt & 1u, wc, SITE_S_FULL);
                 ok = __all_sync(0xffffffffu, ok);
@@ -521,7 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) s[q * 32 + i] = __uint_as_float(sr[q][i]);
                 const int col0 = j * kBN;
-                if (col0 + kBN > tile_vis_min) {  // diagonal or key-tail block
+                const bool masked = col0 + kBN > tile_vis_min;  // diagonal or key-tail block
+                if (masked) {
                     const int lim = vis_end - col0;
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
@@ -529,30 +569,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-                for (int c = 4; c < 128; c += 4) {
-                    mx0 = fmaxf(mx0, s[c]);
-                    mx1 = fmaxf(mx1, s[c + 1]);
-                    mx2 = fmaxf(mx2, s[c + 2]);
-                    mx3 = fmaxf(mx3, s[c + 3]);
+                for (int c = 4; c < 124; c += 8) {
+                    mx0 = max3f(mx0, s[c], s[c + 1]);
+                    mx1 = max3f(mx1, s[c + 2], s[c + 3]);
+                    mx2 = max3f(mx2, s[c + 4], s[c + 5]);
+                    mx3 = max3f(mx3, s[c + 6], s[c + 7]);
                 }
+                mx0 = max3f(mx0, s[124], s[125]);
+                mx1 = max3f(mx1, s[126], s[127]);
                 const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
                 // Lazy rescale: the reference max moves only when it grows by more than
-                // 2^kTau.  tcgen05.ld/st are warp-collective (.sync.aligned), so the O
+                // 2^tau.  tcgen05.ld/st are warp-collective (.sync.aligned), so the O
                 // round trip is taken by the whole warp whenever any of its rows needs it;
                 // rows that keep their reference scale by 1.
-                const bool grow = m_cand > m_run + kTau;
+                const bool grow = m_cand > m_run + lazy_tau<FP8>();
                 if (__any_sync(0xffffffffu, grow)) {
                     const float f = grow ? ex2_approx(m_run - m_cand) : 1.0f;  // 0 if m_run = -inf
                     if (j != j_first) {  // the first block's PV overwrites O (uniform per warp)
+                        const uint64_t f2 = f32x2(f, f);
 #pragma unroll 1
-                        for (int c = 0; c < D; c += 16) {
-                            uint32_t orr[16];
-                            tmem_ld16(t_o + c, orr);
+                        for (int c = 0; c < D; c += 32) {
+                            uint32_t orr[32];
+                            tmem_ld32(t_o + c, orr);
                             tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                orr[i] = __float_as_uint(__uint_as_float(orr[i]) * f);
-                            tmem_st16(t_o + c, orr);
+                            for (int i = 0; i < 32; i += 2) {
+                                float a, b;
+                                unpack_f32x2(mul_f32x2(f32x2(__uint_as_float(orr[i]),
+                                                             __uint_as_float(orr[i + 1])), f2), a, b);
+                                orr[i] = __float_as_uint(a);
+                                orr[i + 1] = __float_as_uint(b);
+                            }
+                            tmem_st32(t_o + c, orr);
                         }
                     }
                     if (grow) {
@@ -561,37 +609,69 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const float mu = (m_run == -INFINITY) ? 0.0f : m_run;
-                float ls0 = 0.f, ls1 = 0.f;
-                if constexpr (FP8) {
-                    uint32_t pk[32];
+                // exp2(s * scale_log2 - mu) on packed fp32 pairs (f32x2 FMA/add halve the
+                // issue slots); P is converted to bf16x2 / e4m3x4 and stored to TMEM in one go.
+                const uint64_t sc2 = f32x2(scale_log2, scale_log2);
+                const uint64_t nm2 = f32x2(-mu, -mu);
+                const uint64_t mg2 = f32x2(kRoundMagic, kRoundMagic);
+                const uint64_t c0 = f32x2(kExp2C0, kExp2C0), c1 = f32x2(kExp2C1, kExp2C1);
+                const uint64_t c2 = f32x2(kExp2C2, kExp2C2), c3 = f32x2(kExp2C3, kExp2C3);
+                uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
+                constexpr int kPkPerChunk = FP8 ? 8 : 16;
+                uint32_t pk_all[4 * kPkPerChunk];
 #pragma unroll
-                    for (int c = 0; c < 128; c += 4) {
-                        const float e0 = ex2_approx(fmaf(s[c], scale_log2, -mu));
-                        const float e1 = ex2_approx(fmaf(s[c + 1], scale_log2, -mu));
-                        const float e2 = ex2_approx(fmaf(s[c + 2], scale_log2, -mu));
-                        const float e3 = ex2_approx(fmaf(s[c + 3], scale_log2, -mu));
-                        ls0 += e0 + e2;
-                        ls1 += e1 + e3;
-                        pk[c / 4] = pack_e4m3x4(e0, e1, e2, e3);
-                    }
-                    tmem_st32(t_s, pk);
-                } else {
-                    uint32_t pk[64];
+                for (int q = 0; q < 4; ++q) {
+                    float e[32];
 #pragma unroll
-                    for (int c = 0; c < 128; c += 2) {
-                        const float e0 = ex2_approx(fmaf(s[c], scale_log2, -mu));
-                        const float e1 = ex2_approx(fmaf(s[c + 1], scale_log2, -mu));
-                        ls0 += e0;
-                        ls1 += e1;
-                        pk[c / 2] = pack_bf16x2(e0, e1);
+                    for (int i = 0; i < 16; ++i) {
+                        const int c = 32 * q + 2 * i;
+                        float a, b;
+                        const uint64_t x2 = fma_f32x2(f32x2(s[c], s[c + 1]), sc2, nm2);
+                        if (FA_EXP2_EMU_PAIRS > 0 && !masked && (i % 16) < FA_EXP2_EMU_PAIRS) {
+                            unpack_f32x2(x2, a, b);
+                            const uint64_t xc = f32x2(fmaxf(a, -125.0f), fmaxf(b, -125.0f));
+                            const uint64_t r = add_f32x2(xc, mg2);          // magic + round(x)
+                            const uint64_t fr = sub_f32x2(xc, sub_f32x2(r, mg2));
+                            uint64_t pp = fma_f32x2(c3, fr, c2);
+                            pp = fma_f32x2(pp, fr, c1);
+                            pp = fma_f32x2(pp, fr, c0);
+                            float p0, p1, r0, r1;
+                            unpack_f32x2(pp, p0, p1);
+                            unpack_f32x2(r, r0, r1);
+                            e[2 * i] = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(r0) << 23));
+                            e[2 * i + 1] = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(r1) << 23));
+                        } else {
+                            unpack_f32x2(x2, a, b);
+                            e[2 * i] = ex2_approx(a);
+                            e[2 * i + 1] = ex2_approx(b);
+                        }
+                        if (i & 1)
+                            acc1 = add_f32x2(acc1, f32x2(e[2 * i], e[2 * i + 1]));
+                        else
+                            acc0 = add_f32x2(acc0, f32x2(e[2 * i], e[2 * i + 1]));
                     }
-                    tmem_st32(t_s, *reinterpret_cast<const uint32_t(*)[32]>(pk));
-                    tmem_st32(t_s + 32u, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+                    uint32_t pk[kPkPerChunk];
+#pragma unroll
+                    for (int i = 0; i < kPkPerChunk; ++i) {
+                        if constexpr (FP8)
+                            pk[i] = pack_e4m3x4(e[4 * i], e[4 * i + 1], e[4 * i + 2], e[4 * i + 3]);
+                        else
+                            pk[i] = pack_bf16x2(e[2 * i], e[2 * i + 1]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < kPkPerChunk; ++i) pk_all[q * kPkPerChunk + i] = pk[i];
                 }
-                l_run += ls0 + ls1;
+                tmem_st32(t_s, *reinterpret_cast<const uint32_t(*)[32]>(pk_all));
+                if constexpr (!FP8)
+                    tmem_st32(t_s + 32u, *reinterpret_cast<const uint32_t(*)[32]>(pk_all + 32));
+                float l0, l1, l2, l3;
+                unpack_f32x2(acc0, l0, l1);
+                unpack_f32x2(acc1, l2, l3);
+                l_run += (l0 + l1) + (l2 + l3);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(C::P_FULL + t));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::P_FULL + t));
             }
             if (aborted) break;
             // ---------------- epilogue: O = O_acc / l, LSE = ln2 * (m + log2 l)
@@ -633,7 +713,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(bar(C::O_EMPTY + t));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::O_EMPTY + t));
             if (row_ok)
                 *lse_ptr = has_mass ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
         }
