@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(C::DRAIN), 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar(C::KV_FULL + s), 1);
-            mbar_init(bar(C::KV_EMPTY + s), 1);
+            mbar_init(bar(C::KV_EMPTY + s), kTiles);  // one release per query tile
         }
         *abort_flag = 0u;
         fence_barrier_init();
@@ -405,12 +405,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j0 < hi0) {
                     issue_qk(std::integral_constant<int, 0>{}, kslot0);
                     umma_commit(bar(C::S_FULL + 0));
+                } else {
+                    mbar_arrive(bar(C::KV_EMPTY + kslot0));  // tile 0 never reads K(j0)
                 }
                 if (j0 < hi1) {
                     issue_qk(std::integral_constant<int, 1>{}, kslot0);
                     umma_commit(bar(C::S_FULL + 1));
+                } else {
+                    mbar_arrive(bar(C::KV_EMPTY + kslot0));
                 }
-                umma_commit(bar(C::KV_EMPTY + kslot0));
                 for (int j = j0; j >= lo; --j) {
                     const uint32_t vslot = ring % C::kStages;
                     if (!wait_bar(bar(C::KV_FULL + vslot), (ring / C::kStages) & 1u, wc, SITE_KV_FULL)) {
@@ -418,6 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     ++ring;
+                    // a tile that does not visit block j releases V(j) at once (its load has
+                    // landed, so the arrival belongs to this phase of the slot)
+                    if (j >= hi0) mbar_arrive(bar(C::KV_EMPTY + vslot));
+                    if (j >= hi1) mbar_arrive(bar(C::KV_EMPTY + vslot));
                     const bool has_next = j - 1 >= lo;
                     const uint32_t nslot = ring % C::kStages;
                     const uint32_t nph = (ring / C::kStages) & 1u;
@@ -455,8 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         aborted = true;
                         break;
                     }
-                    umma_commit(bar(C::KV_EMPTY + vslot));
-                    if (has_next) umma_commit(bar(C::KV_EMPTY + nslot));
+                    if (has_next) {  // K(j-1) has landed (some tile read it); skipping tiles release it
+                        if (j - 1 >= hi0) mbar_arrive(bar(C::KV_EMPTY + nslot));
+                        if (j - 1 >= hi1) mbar_arrive(bar(C::KV_EMPTY + nslot));
+                    }
                 }
                 if (aborted) break;
                 if (has0) umma_commit(bar(C::Q_EMPTY + 0));
@@ -489,11 +498,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             o_scale = p.v_descale ? __ldg(p.v_descale) : 1.0f;
         }
         uint32_t s_cnt = 0, o_cnt = 0;
+        uint32_t kv_base = 0;  // ring position of the current item's first K/V load
+        const bool releaser = wq == 0 && lane == 0;  // this warpgroup's slot-release thread
         bool aborted = false;
         for (int round = 0; !aborted; ++round) {
             const int w = item_of_round(round, nctas);
             if (w >= p.n_items) break;
             const Item it = decode_item(p, w);
+            const uint32_t item_base = kv_base;
+            if (it.n_hi > it.n_lo) kv_base += 2u * (uint32_t)(it.n_hi - it.n_lo);
+            // ring slots of this item's K(j) and V(j)
+            auto k_slot = [&](int j) { return (item_base + 2u * (uint32_t)(it.n_hi - 1 - j)) % C::kStages; };
+            auto v_slot = [&](int j) { return (item_base + 2u * (uint32_t)(it.n_hi - 1 - j) + 1u) % C::kStages; };
             // this warpgroup's tile, selected without indexing (keeps Item in registers)
             const bool t_active = t ? it.active[1] : it.active[0];
             const int t_m0 = t ? it.m0[1] : it.m0[0];
@@ -550,6 +566,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++s_cnt;
                 tc_fence_after();
+                // S_t(j) is complete: K(j) is consumed, and so is V(j+1) (PV_t(j+1) was issued
+                // before S_t(j) by the same thread, and MMAs complete in issue order)
+                if (releaser) {
+                    mbar_arrive(bar(C::KV_EMPTY + k_slot(j)));
+                    if (j + 1 < t_hi) mbar_arrive(bar(C::KV_EMPTY + v_slot(j + 1)));
+                }
                 uint32_t sr[4][32];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) tmem_ld32(t_s + 32u * q, sr[q]);
@@ -685,6 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++o_cnt;
             }
             tc_fence_after();
+            if (releaser) mbar_arrive(bar(C::KV_EMPTY + v_slot(it.n_lo)));  // PV_t(n_lo) is complete
             const bool has_mass = l_run > 0.0f;
             const float inv_l = has_mass ? o_scale / l_run : 0.0f;
 #pragma unroll 1
