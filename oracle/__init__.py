@@ -26,6 +26,9 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "_attn_oracle.so")
+# Tests that plant mistakes in the oracle point this at a mutated build (and skip the
+# rebuild); nothing else sets it.
+_LIB_OVERRIDE = os.environ.get("FA_ORACLE_LIB_OVERRIDE")
 _lock = threading.Lock()
 _lib = None
 
@@ -49,7 +52,7 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            lib = ctypes.CDLL(_LIB_OVERRIDE or build())
             lib.orc_attention_rows.restype = ctypes.c_int
             lib.orc_attention_rows.argtypes = [
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,

@@ -299,3 +299,34 @@ def test_bad_arguments_rejected():
         oracle.attention_rows(q, q, q, np.array([[0, 0, 5]]), softmax_scale=1.0)
     with pytest.raises(ValueError):
         oracle.attention_rows(q, q, q, np.array([[0, 3, 0]]), softmax_scale=1.0)
+
+
+def test_huge_scores_stay_finite_and_match_closed_form():
+    """Scores in the thousands: exp overflows unless the true row max is subtracted.
+    Keys k_j = (j, 1, 0...) and q = (40, 0, ...) give s_j = 40 j * scale; the softmax
+    weights are w_j = exp(s_j - s_max) / sum, the LSE is s_max + ln sum_j exp(s_j - s_max)."""
+    n, d, scale = 9, 4, 7.0
+    q = np.zeros((1, 1, 1, d))
+    q[0, 0, 0, 0] = 40.0
+    k = np.zeros((1, n, 1, d))
+    k[0, :, 0, 0] = np.arange(n)
+    k[0, :, 0, 1] = 1.0
+    v = np.zeros((1, n, 1, 2))
+    v[0, :, 0, 0] = np.arange(n) * 1.5 - 3.0
+    v[0, :, 0, 1] = 1.0
+    s = [40.0 * j * scale for j in range(n)]   # up to 2240
+    smax = max(s)
+    z = sum(math.exp(x - smax) for x in s)
+    o, lse = oracle.attention(q, k, v, softmax_scale=scale)
+    assert np.all(np.isfinite(o)) and np.isfinite(lse).all()
+    assert lse[0, 0, 0] == pytest.approx(smax + math.log(z), rel=1e-14)
+    expect0 = sum(math.exp(x - smax) * (j * 1.5 - 3.0) for j, x in enumerate(s)) / z
+    assert o[0, 0, 0, 0] == pytest.approx(expect0, abs=1e-12)
+    assert o[0, 0, 0, 1] == pytest.approx(1.0, abs=1e-14)
+    # causal, Sq = Sk: row i sees keys 0..i, so the newest key dominates every row
+    qq = np.repeat(q, n, axis=1)
+    o2, lse2 = oracle.attention(qq, k, v, softmax_scale=scale, causal=True)
+    assert np.all(np.isfinite(o2)) and np.all(np.isfinite(lse2))
+    for i in range(n):
+        zi = sum(math.exp(s[j] - s[i]) for j in range(i + 1))
+        assert lse2[0, 0, i] == pytest.approx(s[i] + math.log(zi), rel=1e-14)
