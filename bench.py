@@ -75,6 +75,23 @@ def _recorded_traffic(workload: str):
     return rec.get("bytes_per_launch")
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The slowest rank's value (all_reduce MAX); identity when not distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job rate: every rank processed `units_per_rank` per step (weak scaling),
+    over the slowest rank's time."""
+    return world * units_per_rank * steps / (max_ms * 1e-3)
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -289,13 +306,9 @@ def run_gpu(args, w):
         dist.barrier()
     clocks = sampler.stop()
     times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(times_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(times_ms), dev)
     flops = _flops(w, x)
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(flops, world, args.steps, total_ms) / 1e12
     ms_per_step = total_ms / args.steps
 
     # ---------------- end to end through the public API, host buffers
@@ -330,14 +343,10 @@ def run_gpu(args, w):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
         d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
-        e2e = {"value": world * flops * n_e2e / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_throughput(flops, world, n_e2e, e2e_ms) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms / n_e2e}
 
