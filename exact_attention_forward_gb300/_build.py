@@ -32,19 +32,23 @@ def _deps():
         os.path.join(ROOT, "include", "fa.h")]
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if (not force and os.path.exists(LIB)
-            and os.path.getmtime(LIB) >= max(os.path.getmtime(d) for d in _deps())):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: str = LIB,
+          build_dir: str = BUILD) -> str:
+    """Build the library; `extra_flags` / `lib_path` / `build_dir` make a variant build
+    (e.g. a compile-time option) elsewhere without touching the default library."""
+    if (not force and os.path.exists(lib_path)
+            and os.path.getmtime(lib_path) >= max(os.path.getmtime(d) for d in _deps())):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-                     "-I", os.path.join(ROOT, "include"), "-I", CSRC]
+                     "-Xcompiler", "-fvisibility=hidden",
+                     "-I", os.path.join(ROOT, "include"), "-I", CSRC] + list(extra_flags)
     if verbose:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -56,13 +60,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if verbose:
         for _, log in results:
             print(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -36,6 +36,15 @@
 #include <stddef.h>
 #include <stdint.h>
 
+/* Only the entry points below are exported; the library is built with hidden
+ * visibility, so two builds loaded into one process never bind to each other's
+ * internals. */
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -82,7 +91,7 @@ typedef enum {
  *   FA_ERR_WORKSPACE.  Fixed-length inputs only; ignored for varlen.
  * stream: cudaStream_t.
  */
-fa_status fa_fwd(const void* q, const void* k, const void* v,
+FA_API fa_status fa_fwd(const void* q, const void* k, const void* v,
                  void* o, float* lse,
                  int batch, int heads, int seqlen_q, int seqlen_k,
                  const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
@@ -99,11 +108,11 @@ fa_status fa_fwd(const void* q, const void* k, const void* v,
  * split).  Splitting follows the log-sum-exp merge identity: each split
  * writes a normalised partial O and its LSE, a second kernel merges them.
  */
-size_t fa_fwd_workspace_size(int batch, int heads, int seqlen_q, int seqlen_k,
+FA_API size_t fa_fwd_workspace_size(int batch, int heads, int seqlen_q, int seqlen_k,
                              int head_dim_v, int causal);
 
 /* Number of key splits fa_fwd would use for that shape with a workspace. */
-int fa_fwd_num_splits(int batch, int heads, int seqlen_q, int seqlen_k, int causal);
+FA_API int fa_fwd_num_splits(int batch, int heads, int seqlen_q, int seqlen_k, int causal);
 
 /*
  * fa_fwd_static_workspace -- fa_fwd for fixed-length inputs, for callers that
@@ -123,7 +132,7 @@ int fa_fwd_num_splits(int batch, int heads, int seqlen_q, int seqlen_k, int caus
  * the array's device address, so make it before any stream capture.  This
  * entry point itself allocates nothing.
  */
-fa_status fa_fwd_static_workspace(const void* q, const void* k, const void* v,
+FA_API fa_status fa_fwd_static_workspace(const void* q, const void* k, const void* v,
                                   void* o, float* lse,
                                   int batch, int heads, int seqlen_q, int seqlen_k,
                                   int head_dim, int head_dim_v, float softmax_scale, int causal,
@@ -133,10 +142,10 @@ fa_status fa_fwd_static_workspace(const void* q, const void* k, const void* v,
                                   void* stream);
 
 /* Static description of a status code. */
-const char* fa_status_string(fa_status status);
+FA_API const char* fa_status_string(fa_status status);
 
 /* Thread-local message describing the last non-OK status of this thread. */
-const char* fa_last_error_detail(void);
+FA_API const char* fa_last_error_detail(void);
 
 /*
  * Device-side failure detection.  Every wait inside the kernels is bounded
@@ -148,7 +157,7 @@ const char* fa_last_error_detail(void);
  * timeout) and, if clear != 0, resets it.  Returns FA_ERR_DEVICE_TIMEOUT if
  * a timeout bit was set, FA_OK otherwise (FA_ERR_CUDA on a CUDA failure).
  */
-fa_status fa_device_error(uint32_t* flags, int clear);
+FA_API fa_status fa_device_error(uint32_t* flags, int clear);
 
 /*
  * Debug controls for the failure-detection tests (process-wide, host side,
@@ -156,7 +165,7 @@ fa_status fa_device_error(uint32_t* flags, int clear);
  * inject: 0 = none; 1 = the TMA producer withholds the first Q-tile arrival
  * of each CTA, so the MMA issuer's bounded wait runs out (no GPU fault).
  */
-void fa_debug_set(uint64_t wait_limit_ns, uint32_t inject);
+FA_API void fa_debug_set(uint64_t wait_limit_ns, uint32_t inject);
 
 #ifdef __cplusplus
 }

@@ -215,7 +215,10 @@ def test_bounded_wait_timeout_is_reported_and_context_survives():
     finally:
         fa.debug_set(0, 0)
     assert st == fa.FA_ERR_DEVICE_TIMEOUT
-    assert flags & 1 and (flags >> 8) & 0xFF == 3  # site: MMA issuer waiting for Q
+    # the first wait to give up is one that depends on the withheld Q arrival: the MMA
+    # issuer's Q wait (3), the softmax's S wait (7), or, later in the chain, a K/V ring
+    # wait (2, 4) -- which one wins the race to the limit is not fixed
+    assert flags & 1 and (flags >> 8) & 0xFF in (2, 3, 4, 7)
     # the context is still usable and results are right again
     o, lse = fa.fwd(x["q"], x["k"], x["v"])
     torch.cuda.synchronize()
