@@ -7,7 +7,8 @@ Prints ONE JSON line (rank 0).  A step is one forward pass over the whole
 workload (default: bf16, causal, B=2 H=32 S=8192 D=128, inputs 2*N(0,1)):
 `value` is TFLOP/s with inputs resident in HBM, counted as 4*B*H*Sq*Sk*D
 (halved for causal), timed per step with CUDA events on the launching stream
-and the L2 flushed (a 256 MiB write) between timed steps; `e2e` is the same
+and the L2 flushed between timed steps (a 256 MiB write, then a 256 MiB read so no
+dirty lines are left to write back during the timed step); `e2e` is the same
 metric through the public API with pinned host inputs copied in and O/LSE
 copied out inside the timed region.  Under torchrun each rank runs the same
 workload on its own GPU (the pass shards over independent (batch, head)
@@ -273,7 +274,14 @@ def run_gpu(args, w):
             ws = torch.empty(need, dtype=torch.uint8, device=dev)
     splits = fa.num_splits(w.batch, w.heads, w.seqlen_q, w.seqlen_k, w.causal) if ws is not None else 1
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def flush_l2():
+        # evict the previous step's working set: write 256 MiB, then read another 256 MiB
+        # so the dirty lines are written back before (not during) the timed step
+        flush.zero_()
+        flush_rd.max()
 
     def step():
         fa.fwd(q, k, v, causal=w.causal, softmax_scale=w.softmax_scale, cu_seqlens_q=cu_q,
@@ -281,7 +289,7 @@ def run_gpu(args, w):
                descale=descale, workspace=ws, out=o, lse=lse, stream=stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize()
     st, flags = fa.device_error(clear=True)
@@ -297,7 +305,7 @@ def run_gpu(args, w):
     sampler.start()
     time.sleep(0.3)
     for i in range(args.steps):
-        flush.zero_()  # evict the previous step's working set from L2 (not timed)
+        flush_l2()  # not timed
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -377,7 +385,7 @@ def run_gpu(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if not fp8 else "e4m3", "data": "synthetic",
-        "config": _config(w, "flushed between timed steps (256 MiB write)"),
+        "config": _config(w, "flushed between timed steps (256 MiB write + 256 MiB read, untimed)"),
         "clocks": clocks, "e2e": e2e,
         "gpu_launches": args.steps * (2 if splits > 1 else 1),
         "roofline": roofline,

@@ -185,10 +185,12 @@ def fwd(q, k, v, *, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
             ds[i] = x
     ws = None
     ws_bytes = 0
-    if workspace == "auto":
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError('workspace must be "auto", None or a uint8 CUDA tensor')
         if not varlen:
             need = workspace_size(batch, heads, sq_arg, sk_arg, dv, causal)
-            if need > 0:
+            if need > 0:  # allocated from torch's caching allocator (no cudaMalloc per call)
                 ws = torch.empty(need, dtype=torch.uint8, device=dev)
                 ws_bytes = need
                 temps.append(ws)

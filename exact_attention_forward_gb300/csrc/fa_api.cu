@@ -113,44 +113,96 @@ size_t workspace_bytes_for(int splits, int batch, int heads, int sq, int dv) {
 }  // namespace
 
 // ---------------------------------------------------------------- split merge
-// One warp per output row: LSE = ln sum_s exp(LSE_s); O = sum_s exp(LSE_s - LSE) O_s.
+// One warp per output row.  LSE = ln sum_s exp(LSE_s) and O = sum_s exp(LSE_s - LSE) O_s.
+// Lanes own splits for the LSE reductions (warp shuffles; for <= 32 splits each lane keeps
+// its weight in a register and broadcasts it), then own 4 (Dv = 128) or 2 (Dv = 64)
+// columns of O; the split loop is unrolled so several partial rows are in flight at once.
+template <int DV>
 __global__ void __launch_bounds__(256) fa_combine_kernel(const float* __restrict__ ws_o,
                                                          const float* __restrict__ ws_lse,
                                                          __nv_bfloat16* __restrict__ o,
                                                          float* __restrict__ lse, int batch,
-                                                         int heads, int sq, int dv, int splits) {
-    const int warp = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
+                                                         int heads, int sq, int splits) {
+    constexpr int kCols = DV / 32;  // columns per lane
     const long long rows = (long long)batch * heads * sq;
-    if (warp >= rows) return;
-    const int i = warp % sq;
-    const int bh = warp / sq;
-    const int h = bh % heads;
-    const int b = bh / heads;
+    const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const int i = (int)(row % sq);
+    const long long bh = row / sq;
+    const int h = (int)(bh % heads);
+    const long long b = bh / heads;
     const size_t stride = (size_t)rows;  // rows per split
+    // launched as a programmatic dependent of the forward kernel: wait for its
+    // completion (and memory) before reading the partial results
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float mx = -INFINITY;
-    for (int s = 0; s < splits; ++s) mx = fmaxf(mx, ws_lse[s * stride + warp]);
-    const size_t out_row = (((size_t)b * sq + i) * heads + h) * dv;
-    if (mx == -INFINITY) {
-        for (int c = lane * 2; c < dv; c += 64)
-            *reinterpret_cast<__nv_bfloat162*>(o + out_row + c) = __floats2bfloat162_rn(0.f, 0.f);
-        if (lane == 0) lse[((size_t)b * heads + h) * sq + i] = -INFINITY;
+    for (int s = lane; s < splits; s += 32) mx = fmaxf(mx, __ldg(ws_lse + s * stride + row));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    __nv_bfloat16* out = o + (((size_t)b * sq + i) * heads + h) * DV + lane * kCols;
+    float* lse_out = lse + ((size_t)b * heads + h) * sq + i;
+    if (mx == -INFINITY) {  // no split saw a key: O = 0, LSE = -inf
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) out[c] = __float2bfloat16(0.f);
+        if (lane == 0) *lse_out = -INFINITY;
         return;
     }
-    float tot = 0.f;
-    for (int s = 0; s < splits; ++s) tot += expf(ws_lse[s * stride + warp] - mx);
-    const float inv = 1.0f / tot;
-    for (int c = lane * 2; c < dv; c += 64) {
-        float a0 = 0.f, a1 = 0.f;
-        for (int s = 0; s < splits; ++s) {
-            const float w = expf(ws_lse[s * stride + warp] - mx) * inv;
-            const float2 v = *reinterpret_cast<const float2*>(ws_o + (s * stride + warp) * dv + c);
-            a0 = fmaf(w, v.x, a0);
-            a1 = fmaf(w, v.y, a1);
-        }
-        *reinterpret_cast<__nv_bfloat162*>(o + out_row + c) = __floats2bfloat162_rn(a0, a1);
+    float w_lane = 0.f, tot = 0.f;
+    for (int s = lane; s < splits; s += 32) {
+        const float e = expf(__ldg(ws_lse + s * stride + row) - mx);
+        if (s < 32) w_lane = e;
+        tot += e;
     }
-    if (lane == 0) lse[((size_t)b * heads + h) * sq + i] = mx + logf(tot);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+    const float inv = 1.0f / tot;
+    float acc[kCols];
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
+    const float* src = ws_o + (size_t)row * DV + lane * kCols;
+    // batches of 8 splits: all 8 partial-row loads are issued before any is used
+    constexpr int kBatch = 8;
+    for (int s0 = 0; s0 < splits; s0 += kBatch) {
+        float v[kBatch][kCols];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int s = s0 + u;
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) v[u][c] = 0.f;
+            if (s < splits) {
+                if constexpr (kCols == 4) {
+                    const float4 t = __ldg(reinterpret_cast<const float4*>(src + s * stride * DV));
+                    v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+                } else {
+                    const float2 t = __ldg(reinterpret_cast<const float2*>(src + s * stride * DV));
+                    v[u][0] = t.x; v[u][1] = t.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int s = s0 + u;  // uniform across the warp
+            float w = 0.f;
+            if (s < 32)
+                w = __shfl_sync(0xffffffffu, w_lane, s) * inv;  // 0 past the last split
+            else if (s < splits)
+                w = expf(__ldg(ws_lse + s * stride + row) - mx) * inv;
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) acc[c] = fmaf(w, v[u][c], acc[c]);
+        }
+    }
+    if constexpr (kCols == 4) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2], acc[3]);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(out) = pk;
+    } else {
+        *reinterpret_cast<__nv_bfloat162*>(out) = __floats2bfloat162_rn(acc[0], acc[1]);
+    }
+    if (lane == 0) *lse_out = mx + logf(tot);
 }
 
 cudaError_t launch_combine(const float* ws_o, const float* ws_lse, void* o, float* lse, int batch,
@@ -158,9 +210,24 @@ cudaError_t launch_combine(const float* ws_o, const float* ws_lse, void* o, floa
     const long long rows = (long long)batch * heads * seqlen_q;
     const int threads = 256;
     const long long blocks = (rows * 32 + threads - 1) / threads;
-    fa_combine_kernel<<<(unsigned)blocks, threads, 0, s>>>(
-        ws_o, ws_lse, static_cast<__nv_bfloat16*>(o), lse, batch, heads, seqlen_q, dv, n_splits);
-    return cudaGetLastError();
+    // programmatic dependent launch: the merge grid is set up while the forward
+    // kernel drains; griddepcontrol.wait in the merge orders it after the forward
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+    if (dv == 128)
+        return cudaLaunchKernelEx(&cfg, fa_combine_kernel<128>, ws_o, ws_lse, ob, lse, batch, heads,
+                                  seqlen_q, n_splits);
+    return cudaLaunchKernelEx(&cfg, fa_combine_kernel<64>, ws_o, ws_lse, ob, lse, batch, heads,
+                              seqlen_q, n_splits);
 }
 
 }  // namespace fa

@@ -744,6 +744,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     __syncthreads();
+    // lets a programmatically dependent grid (the split merge) be scheduled; it still
+    // waits for this grid's completion before reading anything
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();

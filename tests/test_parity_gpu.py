@@ -165,6 +165,17 @@ def test_split_causal_small():
     compare(o, lse, o_ref, lse_ref, what="split causal")
 
 
+@pytest.mark.parametrize("D", [128, 64])
+def test_many_splits(D):
+    # one (batch, head) and a long key range: more than 32 key splits, so the merge's
+    # per-split weights no longer fit one per lane
+    x = inputs.make_random(1, 1, 100, 40000, D, seed=43 + D)
+    assert fa.num_splits(1, 1, 100, 40000) > 32
+    o, lse = run_gpu(x, causal=False, softmax_scale=D ** -0.5)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=D ** -0.5)
+    compare(o, lse, o_ref, lse_ref, what=f"many splits D={D}")
+
+
 def test_zero_keys_fixed_length():
     x = inputs.make_random(2, 2, 130, 0, 128, seed=3)
     o, lse = run_gpu(x, causal=False, softmax_scale=0.1)
