@@ -57,7 +57,7 @@ def _load():
             lib.orc_attention_rows.argtypes = [
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                 ctypes.c_double, ctypes.c_double, ctypes.c_double,
-                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_void_p, ctypes.c_void_p,
                 ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
                 ctypes.c_void_p, ctypes.c_int64,
@@ -118,7 +118,8 @@ def attention_rows(q, k, v, rows, *, softmax_scale, causal=False,
     """Evaluate the given (b, h, i) query rows.
 
     q, k, v: torch tensors (bf16, float8_e4m3fn or any float -> fp64) or numpy
-    arrays, fixed-length [B, S, H, D] or packed [total, H, D] with cu_seqlens.
+    arrays, fixed-length [B, S, H, D] or packed [total, H, D] with cu_seqlens;
+    K/V may have fewer heads than Q (grouped-query attention).
     Returns (O [n, Dv] fp64, LSE [n] fp64[, P [n, max Sk] fp64]).
     """
     qa, dq = _as_storage(q)
@@ -133,6 +134,7 @@ def attention_rows(q, k, v, rows, *, softmax_scale, causal=False,
         ck = np.ascontiguousarray(np.asarray(cu_seqlens_k, dtype=np.int32))
         batch = cq.size - 1
         heads, d = qa.shape[1], qa.shape[2]
+        heads_k = ka.shape[1]
         dv = va.shape[2]
         sq = sk = 0
         max_sk = int(np.max(ck[1:] - ck[:-1])) if batch > 0 else 0
@@ -140,6 +142,7 @@ def attention_rows(q, k, v, rows, *, softmax_scale, causal=False,
     else:
         batch, sq, heads, d = qa.shape
         sk = ka.shape[1]
+        heads_k = ka.shape[2]
         dv = va.shape[3]
         max_sk = sk
         cq_p = ck_p = None
@@ -150,7 +153,7 @@ def attention_rows(q, k, v, rows, *, softmax_scale, causal=False,
     rc = _load().orc_attention_rows(
         qa.ctypes.data, ka.ctypes.data, va.ctypes.data, dq,
         float(descale[0]), float(descale[1]), float(descale[2]),
-        int(batch), int(heads), int(sq), int(sk), cq_p, ck_p,
+        int(batch), int(heads), int(heads_k), int(sq), int(sk), cq_p, ck_p,
         int(d), int(dv), float(softmax_scale), int(bool(causal)),
         rows.ctypes.data, n, o.ctypes.data, lse.ctypes.data,
         None if p is None else p.ctypes.data, 0 if p is None else p.shape[1])

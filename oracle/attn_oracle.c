@@ -26,6 +26,10 @@
  * epilogue in the page "FlashAttention core algorithm: forward pass"
  * (epilogue excerpt: all-zero O, -inf LSE).
  *
+ * Grouped-query attention: K and V may have fewer heads (heads_k) than Q;
+ * query head h reads key/value head h / (heads / heads_k).  heads_k = heads is
+ * ordinary multi-head attention.
+ *
  * FP8 inputs: the page "FlashAttention core algorithm: forward pass"
  * (consumer mainloop excerpt, FP8 branch) folds q_descale * k_descale into
  * the softmax scale and the output is scaled by the V descale.  Both are the
@@ -33,8 +37,8 @@
  * this oracle does: every input element is decoded exactly to fp64 and
  * multiplied by its tensor's descale in fp64.
  *
- * Layouts: fixed length   Q [B, Sq, H, D], K/V [B, Sk, H, D]
- *          packed varlen  Q [total_q, H, D], K/V [total_k, H, D] with
+ * Layouts: fixed length   Q [B, Sq, H, D], K/V [B, Sk, Hk, D]
+ *          packed varlen  Q [total_q, H, D], K/V [total_k, Hk, D] with
  *                         cu_seqlens (host int32 [B + 1]).
  * The caller chooses which rows to evaluate as (b, h, i) triples.
  */
@@ -96,7 +100,7 @@ int orc_decode(int dtype, const void* src, double* dst, int64_t n) {
  */
 int orc_attention_rows(const void* q, const void* k, const void* v, int dtype,
                        double q_descale, double k_descale, double v_descale,
-                       int batch, int heads, int seqlen_q, int seqlen_k,
+                       int batch, int heads, int heads_k, int seqlen_q, int seqlen_k,
                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
                        int d, int dv, double softmax_scale, int causal,
                        const int64_t* rows, int64_t n_rows,
@@ -104,6 +108,8 @@ int orc_attention_rows(const void* q, const void* k, const void* v, int dtype,
                        double* p_out, int64_t p_stride) {
     if (!q || !k || !v || !rows || !o_out || !lse_out) return 1;
     if (dtype < ORC_F64 || dtype > ORC_E4M3 || batch < 0 || heads < 1 || d < 1 || dv < 1) return 1;
+    if (heads_k < 1 || heads % heads_k != 0) return 1;
+    const int group = heads / heads_k;  /* query heads per key/value head */
     if ((cu_seqlens_q == NULL) != (cu_seqlens_k == NULL)) return 1;
     int varlen = cu_seqlens_q != NULL;
     for (int64_t r = 0; r < n_rows; ++r) {
@@ -146,9 +152,10 @@ int orc_attention_rows(const void* q, const void* k, const void* v, int dtype,
         }
         double* s = (double*)malloc(sizeof(double) * (size_t)n_vis);
         int64_t q_off = (q_row * heads + h) * (int64_t)d;
+        const int64_t hk = h / group;  /* the key/value head this query head reads */
         /* scores */
         for (int64_t j = 0; j < n_vis; ++j) {
-            int64_t k_off = ((k_row0 + j) * heads + h) * (int64_t)d;
+            int64_t k_off = ((k_row0 + j) * heads_k + hk) * (int64_t)d;
             double acc = 0.0;
             for (int c = 0; c < d; ++c)
                 acc += (orc_load(q, dtype, q_off + c) * q_descale) *
@@ -165,7 +172,7 @@ int orc_attention_rows(const void* q, const void* k, const void* v, int dtype,
         for (int64_t j = 0; j < n_vis; ++j) {
             double p = exp(s[j] - m) / l;
             if (p_row) p_row[j] = p;
-            int64_t v_off = ((k_row0 + j) * heads + h) * (int64_t)dv;
+            int64_t v_off = ((k_row0 + j) * heads_k + hk) * (int64_t)dv;
             for (int c = 0; c < dv; ++c)
                 o_row[c] += p * (orc_load(v, dtype, v_off + c) * v_descale);
         }

@@ -27,10 +27,13 @@ MUTANTS = {
     "lse_without_max": ("lse_out[r] = m + log(l);", "lse_out[r] = log(l);"),
     "max_over_first_half": ("for (int64_t j = 1; j < n_vis; ++j) if (s[j] > m) m = s[j];",
                             "for (int64_t j = 1; j < n_vis / 2; ++j) if (s[j] > m) m = s[j];"),
-    "v_strided_by_d": ("int64_t v_off = ((k_row0 + j) * heads + h) * (int64_t)dv;",
-                       "int64_t v_off = ((k_row0 + j) * heads + h) * (int64_t)d;"),
-    "k_head_major": ("int64_t k_off = ((k_row0 + j) * heads + h) * (int64_t)d;",
-                     "int64_t k_off = ((int64_t)h * (k_row0 + sk) + k_row0 + j) * (int64_t)d;"),
+    "v_strided_by_d": ("int64_t v_off = ((k_row0 + j) * heads_k + hk) * (int64_t)dv;",
+                       "int64_t v_off = ((k_row0 + j) * heads_k + hk) * (int64_t)d;"),
+    "k_head_major": ("int64_t k_off = ((k_row0 + j) * heads_k + hk) * (int64_t)d;",
+                     "int64_t k_off = ((int64_t)hk * (k_row0 + sk) + k_row0 + j) * (int64_t)d;"),
+    "gqa_head_modulo": ("const int64_t hk = h / group;", "const int64_t hk = h % heads_k;"),
+    "gqa_k_uses_query_head": ("int64_t k_off = ((k_row0 + j) * heads_k + hk) * (int64_t)d;",
+                              "int64_t k_off = ((k_row0 + j) * heads_k + h % heads_k) * (int64_t)d;"),
     "q_row_ignores_batch": ("q_row = b * (int64_t)seqlen_q + i;", "q_row = i;"),
     "v_uses_k": ("o_row[c] += p * (orc_load(v, dtype, v_off + c) * v_descale);",
                  "o_row[c] += p * (orc_load(k, dtype, v_off + c) * v_descale);"),

@@ -25,9 +25,12 @@ pytestmark = pytest.mark.filterwarnings("ignore")
 # an independent brute force: plain Python floats, explicit visible sets
 # --------------------------------------------------------------------------
 def brute_force(q, k, v, scale, causal):
-    """q [B,Sq,H,D], k/v [B,Sk,H,D] nested lists -> O [B,Sq,H,Dv], LSE [B,H,Sq]."""
+    """q [B,Sq,H,D], k/v [B,Sk,Hk,D] nested lists -> O [B,Sq,H,Dv], LSE [B,H,Sq].
+    Query head h reads key/value head h // (H // Hk)."""
     B, Sq, H = len(q), len(q[0]), len(q[0][0])
     Sk = len(k[0])
+    Hk = len(k[0][0]) if Sk else H
+    grp = H // Hk
     Dv = len(v[0][0][0]) if Sk else 0
     O = [[[None] * H for _ in range(Sq)] for _ in range(B)]
     L = [[[None] * Sq for _ in range(H)] for _ in range(B)]
@@ -39,10 +42,11 @@ def brute_force(q, k, v, scale, causal):
                     O[b][i][h] = [0.0] * len(v[0][0][0]) if Sk else [0.0]
                     L[b][h][i] = -math.inf
                     continue
-                s = {j: scale * sum(a * c for a, c in zip(q[b][i][h], k[b][j][h])) for j in vis}
+                hk = h // grp
+                s = {j: scale * sum(a * c for a, c in zip(q[b][i][h], k[b][j][hk])) for j in vis}
                 e = {j: math.exp(s[j]) for j in vis}  # tiny values: no overflow
                 z = sum(e.values())
-                O[b][i][h] = [sum(e[j] * v[b][j][h][c] for j in vis) / z for c in range(Dv)]
+                O[b][i][h] = [sum(e[j] * v[b][j][hk][c] for j in vis) / z for c in range(Dv)]
                 L[b][h][i] = math.log(z)
     return O, L
 
@@ -51,15 +55,18 @@ def _rand(shape, rng):
     return np.asarray(rng.standard_normal(shape), dtype=np.float64)
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(16))
 def test_brute_force_tiny(seed):
     rng = np.random.default_rng(seed)
     B, H = rng.integers(1, 3), rng.integers(1, 4)
+    Hk = H if seed < 10 else 1 if seed % 2 else H  # MHA, and multi-query for some seeds
+    if seed >= 12:
+        H, Hk = 4, 2                                  # grouped-query: 2 query heads per K/V head
     Sq, Sk = int(rng.integers(1, 9)), int(rng.integers(1, 9))
     D, Dv = int(rng.integers(1, 5)), int(rng.integers(1, 5))
     causal = bool(seed % 2)
     scale = float(rng.uniform(0.2, 1.5))
-    q, k, v = _rand((B, Sq, H, D), rng), _rand((B, Sk, H, D), rng), _rand((B, Sk, H, Dv), rng)
+    q, k, v = _rand((B, Sq, H, D), rng), _rand((B, Sk, Hk, D), rng), _rand((B, Sk, Hk, Dv), rng)
     o, lse = oracle.attention(q, k, v, softmax_scale=scale, causal=causal)
     O, L = brute_force(q.tolist(), k.tolist(), v.tolist(), scale, causal)
     O = np.array(O, dtype=np.float64)
@@ -330,3 +337,24 @@ def test_huge_scores_stay_finite_and_match_closed_form():
     for i in range(n):
         zi = sum(math.exp(s[j] - s[i]) for j in range(i + 1))
         assert lse2[0, 0, i] == pytest.approx(s[i] + math.log(zi), rel=1e-14)
+
+
+@pytest.mark.parametrize("H,Hk", [(8, 2), (6, 1), (4, 4)])
+def test_grouped_query_equals_repeated_heads(H, Hk):
+    """Grouped-query attention is multi-head attention over K/V heads repeated so that
+    consecutive query heads share one key/value head."""
+    rng = np.random.default_rng(15 + H + Hk)
+    B, Sq, Sk, D = 2, 7, 11, 5
+    q, k, v = _rand((B, Sq, H, D), rng), _rand((B, Sk, Hk, D), rng), _rand((B, Sk, Hk, D), rng)
+    kr, vr = np.repeat(k, H // Hk, axis=2), np.repeat(v, H // Hk, axis=2)
+    for causal in (False, True):
+        o, lse = oracle.attention(q, k, v, softmax_scale=0.4, causal=causal)
+        o2, lse2 = oracle.attention(q, kr, vr, softmax_scale=0.4, causal=causal)
+        assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+
+
+def test_grouped_query_rejects_indivisible_heads():
+    q = np.zeros((1, 2, 3, 4))
+    k = np.zeros((1, 2, 2, 4))
+    with pytest.raises(ValueError):
+        oracle.attention(q, k, k, softmax_scale=1.0)
