@@ -253,7 +253,8 @@ def run_reference(args, w):
 
 
 def _config(w, l2):
-    c = {"workload": w.name, "batch": w.batch, "heads": w.heads, "seqlen_q": w.seqlen_q,
+    c = {"workload": w.name, "batch": w.batch, "heads": w.heads, "heads_k": w.kv_heads,
+         "seqlen_q": w.seqlen_q,
          "seqlen_k": w.seqlen_k, "head_dim": w.head_dim, "causal": w.causal,
          "input_dtype": w.dtype, "values": f"{w.amp:g}*N(0,1) seed {w.seed}", "l2": l2}
     if w.varlen:

@@ -10,7 +10,8 @@ it raises.
     o, lse = fwd(q, k, v, causal=True)
 
 q, k, v: CUDA tensors, bf16 or float8_e4m3fn, [B, S, H, D] (or packed
-[total, H, D] with cu_seqlens_q / cu_seqlens_k int32 [B + 1] on the device).
+[total, H, D] with cu_seqlens_q / cu_seqlens_k int32 [B + 1] on the device);
+k and v may have fewer heads than q (grouped-query attention).
 Returns o (bf16, q's layout) and lse (fp32, [B, H, Sq] or [H, total_q]).
 """
 from __future__ import annotations
@@ -33,7 +34,7 @@ FA_DTYPE_BF16, FA_DTYPE_E4M3 = 0, 1
 # Every function declared in include/fa.h.
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_num_splits", "fa_status_string",
                     "fa_last_error_detail", "fa_device_error", "fa_debug_set",
-                    "fa_fwd_static_workspace")
+                    "fa_fwd_static_workspace", "fa_fwd_gqa")
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +78,9 @@ def load_library():
         lib.fa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         lib.fa_debug_set.restype = None
         lib.fa_debug_set.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
+        lib.fa_fwd_gqa.restype = i32
+        lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, i32,
+                                   i32, i32, f32, i32, i32, vp, vp, vp, vp, sz, vp]
         lib.fa_fwd_static_workspace.restype = i32
         lib.fa_fwd_static_workspace.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                                 f32, i32, i32, vp, vp, vp, vp]
@@ -147,6 +151,7 @@ def fwd(q, k, v, *, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
     if k.dtype != q.dtype or v.dtype != q.dtype:
         raise ValueError("q, k, v must share one dtype")
     varlen = cu_seqlens_q is not None
+    heads_k = k.shape[-2]
     if varlen:
         total_q, heads, d = q.shape
         total_k = k.shape[0]
@@ -199,8 +204,8 @@ def fwd(q, k, v, *, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
         ws_bytes = workspace.numel() * workspace.element_size()
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    st = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(batch), int(heads),
-                    int(sq_arg), int(sk_arg), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), mq, mk,
+    st = lib.fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(batch), int(heads),
+                    int(heads_k), int(sq_arg), int(sk_arg), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), mq, mk,
                     int(d), int(dv), float(softmax_scale), int(bool(causal)), dt,
                     _ptr(ds[0]), _ptr(ds[1]), _ptr(ds[2]), _ptr(ws), ws_bytes,
                     ctypes.c_void_p(stream.cuda_stream))

@@ -298,6 +298,19 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int head_dim_v, float softmax_scale, int causal, fa_dtype dtype,
                  const float* q_descale, const float* k_descale, const float* v_descale,
                  void* workspace, size_t workspace_bytes, void* stream) {
+    return fa_fwd_gqa(q, k, v, o, lse, batch, heads, heads, seqlen_q, seqlen_k, cu_seqlens_q,
+                      cu_seqlens_k, max_seqlen_q, max_seqlen_k, head_dim, head_dim_v, softmax_scale,
+                      causal, dtype, q_descale, k_descale, v_descale, workspace, workspace_bytes,
+                      stream);
+}
+
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int batch,
+                     int heads, int heads_k, int seqlen_q, int seqlen_k,
+                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int max_seqlen_q,
+                     int max_seqlen_k, int head_dim, int head_dim_v, float softmax_scale,
+                     int causal, fa_dtype dtype, const float* q_descale, const float* k_descale,
+                     const float* v_descale, void* workspace, size_t workspace_bytes,
+                     void* stream) {
     t_detail[0] = '\0';
     // ---------------------------------------------------------------- validation
     const bool varlen = cu_seqlens_q != nullptr || cu_seqlens_k != nullptr;
@@ -309,6 +322,9 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
         return fail(FA_ERR_INVALID_ARG, "q, k, v, o and lse must be 16-byte aligned");
     if (batch < 0 || heads < 1 || seqlen_q < 0 || seqlen_k < 0)
         return fail(FA_ERR_INVALID_ARG, "need batch >= 0, heads >= 1, seqlen_q/k >= 0");
+    if (heads_k < 1 || heads % heads_k != 0)
+        return fail(FA_ERR_INVALID_ARG, "heads_k (%d) must be >= 1 and divide heads (%d)", heads_k,
+                    heads);
     if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
     if (!(softmax_scale > 0.0f) || !std::isfinite(softmax_scale))
         return fail(FA_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
@@ -333,7 +349,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
         return fail(FA_ERR_UNSUPPORTED, "e4m3 head_dim %d not built (128)", head_dim);
     const long long rows_q = varlen ? seqlen_q : (long long)batch * seqlen_q;
     const long long rows_k = varlen ? seqlen_k : (long long)batch * seqlen_k;
-    if (rows_q * heads * head_dim >= (1ll << 40) || rows_k * heads * head_dim >= (1ll << 40))
+    if (rows_q * heads * head_dim >= (1ll << 40) || rows_k * heads_k * head_dim >= (1ll << 40))
         return fail(FA_ERR_INVALID_ARG, "tensor too large");
     if (rows_q >= (1ll << 31) || rows_k >= (1ll << 31))
         return fail(FA_ERR_INVALID_ARG, "row count must fit in int32");
@@ -367,6 +383,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     p.err = err;
     p.batch = batch;
     p.heads = heads;
+    p.kv_group = heads / heads_k;
     p.seqlen_q = mq;
     p.seqlen_k = mk;
     p.total_q = varlen ? seqlen_q : 0;
@@ -402,8 +419,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
         tk = tq;
         tv = tq;
     } else {
-        if ((st = encode_map(&tk, k, fp8, head_dim, heads, seqlen_k, nbat)) != FA_OK) return st;
-        if ((st = encode_map(&tv, v, fp8, head_dim, heads, seqlen_k, nbat)) != FA_OK) return st;
+        if ((st = encode_map(&tk, k, fp8, head_dim, heads_k, seqlen_k, nbat)) != FA_OK) return st;
+        if ((st = encode_map(&tv, v, fp8, head_dim, heads_k, seqlen_k, nbat)) != FA_OK) return st;
     }
 
     // ---------------------------------------------------------------- launch

@@ -135,7 +135,9 @@ struct Item {
 };
 
 // Longest-processing-time order: item index -> pair index descending (under a
-// causal mask later pairs see more key blocks), then (batch, head, split).
+// causal mask later pairs see more key blocks), then (batch, head, split).  Query
+// heads sharing a K/V head (grouped-query attention) are consecutive items, so
+// they stream the same K/V at about the same time and share it in L2.
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int w) {
     Item it;
     const int per_m = p.batch * p.heads * p.n_splits;
@@ -309,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     aborted = true;
                     break;
                 }
+                const int kv_head = it.h / p.kv_group;  // grouped-query: shared K/V head
                 for (int j = it.n_hi - 1; j >= it.n_lo && !aborted; --j) {
                     const int krow = (p.varlen ? it.k_row0 : 0) + j * kBN;
 #pragma unroll
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int c = 0; c < C::kChunks; ++c)
                             tma_load_4d(s_kv + slot * C::kTileBytes + c * C::kChunkBytes,
                                         kv ? &tm_v : &tm_k, bar(C::KV_FULL + slot),
-                                        c * C::kChunkElems, it.h, krow, bc, pol_kv);
+                                        c * C::kChunkElems, kv_head, krow, bc, pol_kv);
                         ++ring;
                     }
                 }

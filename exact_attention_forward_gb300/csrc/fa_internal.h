@@ -22,6 +22,7 @@ struct FwdParams {
     float* ws_lse;              // split mode: partial LSE [splits, B, H, Sq] fp32
     uint32_t* err;              // device error word
     int batch, heads;
+    int kv_group;               // query heads per K/V head (grouped-query attention; 1 = MHA)
     int seqlen_q, seqlen_k;     // fixed length: the lengths; varlen: max lengths
     int total_q;                // varlen: packed rows of Q (LSE row stride)
     int n_mpairs;               // ceil(seqlen_q / 256): query-row pairs of tiles

@@ -13,6 +13,7 @@ Workloads (shapes and value distributions of the attention configurations):
   bf16_varlen_causal  16 seqs, S~U{1..4096}, +2 with Sk=0; H=16 D=128 causal seed 1004
   fp8_noncausal_4k    B=4  H=16 S=4096 D=128 e4m3 per-tensor amax/448  non-causal seed 1005
   bf16_shortq_longkv  B=1  H=8  Sq=128 Sk=65536 D=128 N(0,1) non-causal  seed 1006
+  bf16_gqa_causal_8k  B=2  H=32 (8 K/V heads) S=8192 D=128 2*N(0,1) causal seed 1007
 """
 from __future__ import annotations
 
@@ -40,10 +41,15 @@ class Workload:
     varlen: bool = False         # lengths drawn per sequence (seqlen_q/k = max 4096)
     n_seqs: int = 0
     empty_k_at: tuple = ()       # packed positions of sequences with seqlen_k = 0
+    heads_k: int = 0             # K/V heads (grouped-query attention); 0 = heads
 
     @property
     def softmax_scale(self) -> float:
         return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def kv_heads(self) -> int:
+        return self.heads_k or self.heads
 
 
 WORKLOADS = {
@@ -58,6 +64,9 @@ WORKLOADS = {
                                  dtype="e4m3", seed=1005),
     "bf16_shortq_longkv": Workload("bf16_shortq_longkv", 1, 8, 128, 65536, 128, False,
                                    seed=1006),
+    # grouped-query attention (4 query heads per K/V head) at the 8K causal shape
+    "bf16_gqa_causal_8k": Workload("bf16_gqa_causal_8k", 2, 32, 8192, 8192, 128, True, amp=2.0,
+                                   seed=1007, heads_k=8),
 }
 
 
@@ -113,11 +122,11 @@ def make_inputs(w: Workload, *, seed: Optional[int] = None, shapes_only_q: Optio
         cu_q = torch.tensor([0] + list(_cumsum(sq)), dtype=torch.int32)
         cu_k = torch.tensor([0] + list(_cumsum(sk)), dtype=torch.int32)
         q_shape = (int(cu_q[-1]), w.heads, w.head_dim)
-        k_shape = (int(cu_k[-1]), w.heads, w.head_dim)
+        k_shape = (int(cu_k[-1]), w.kv_heads, w.head_dim)
         max_q, max_k = max(sq), max(sk)
     else:
         q_shape = (w.batch, w.seqlen_q, w.heads, w.head_dim)
-        k_shape = (w.batch, w.seqlen_k, w.heads, w.head_dim)
+        k_shape = (w.batch, w.seqlen_k, w.kv_heads, w.head_dim)
         max_q, max_k = w.seqlen_q, w.seqlen_k
     q = torch.randn(q_shape, generator=gen, dtype=torch.float32)
     k = torch.randn(k_shape, generator=gen, dtype=torch.float32)
@@ -139,21 +148,22 @@ def make_inputs(w: Workload, *, seed: Optional[int] = None, shapes_only_q: Optio
 
 
 def make_random(batch, heads, seqlen_q, seqlen_k, head_dim, *, seed, amp=1.0,
-                dtype="bf16"):
+                dtype="bf16", heads_k=0):
     """Fixed-length N(0,1)*amp inputs of an arbitrary shape (for edge cases)."""
     w = Workload("custom", batch, heads, seqlen_q, seqlen_k, head_dim, False, dtype=dtype,
-                 amp=amp, seed=seed)
+                 amp=amp, seed=seed, heads_k=heads_k)
     return make_inputs(w)
 
 
-def make_varlen(seqlens_q, seqlens_k, heads, head_dim, *, seed, amp=1.0):
+def make_varlen(seqlens_q, seqlens_k, heads, head_dim, *, seed, amp=1.0, heads_k=0):
     """Packed varlen bf16 inputs for given per-sequence lengths."""
     gen = torch.Generator(device="cpu").manual_seed(seed)
     cu_q = torch.tensor([0] + list(_cumsum(seqlens_q)), dtype=torch.int32)
     cu_k = torch.tensor([0] + list(_cumsum(seqlens_k)), dtype=torch.int32)
+    hk = heads_k or heads
     q = torch.randn((int(cu_q[-1]), heads, head_dim), generator=gen) * amp
-    k = torch.randn((int(cu_k[-1]), heads, head_dim), generator=gen) * amp
-    v = torch.randn((int(cu_k[-1]), heads, head_dim), generator=gen) * amp
+    k = torch.randn((int(cu_k[-1]), hk, head_dim), generator=gen) * amp
+    v = torch.randn((int(cu_k[-1]), hk, head_dim), generator=gen) * amp
     return dict(q=q.to(torch.bfloat16), k=k.to(torch.bfloat16), v=v.to(torch.bfloat16),
                 descale=(1.0, 1.0, 1.0), cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
                 max_seqlen_q=max(seqlens_q) if seqlens_q else 0,

@@ -103,6 +103,29 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v,
                  void* stream);
 
 /*
+ * fa_fwd_gqa -- fa_fwd with grouped-query / multi-query attention: K and V have
+ * heads_k heads (heads_k >= 1 dividing heads; heads_k == heads is fa_fwd) and query
+ * head h attends with key/value head h / (heads / heads_k).  Layouts as fa_fwd with
+ * heads_k in place of heads for k and v:
+ *   fixed length  k, v [batch, seqlen_k, heads_k, head_dim]
+ *   varlen        k, v [seqlen_k, heads_k, head_dim]
+ * All other arguments, the outputs and the errors are those of fa_fwd (plus
+ * FA_ERR_INVALID_ARG when heads_k does not divide heads).  Not on the pages: the
+ * same forward pass with the K/V head index shared by a group of query heads.
+ */
+FA_API fa_status fa_fwd_gqa(const void* q, const void* k, const void* v,
+                            void* o, float* lse,
+                            int batch, int heads, int heads_k, int seqlen_q, int seqlen_k,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int max_seqlen_q, int max_seqlen_k,
+                            int head_dim, int head_dim_v, float softmax_scale, int causal,
+                            fa_dtype dtype,
+                            const float* q_descale, const float* k_descale,
+                            const float* v_descale,
+                            void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
  * Bytes of workspace that fa_fwd would use to split the key range of a
  * fixed-length problem of this shape on the current device (0 = it would not
  * split).  Splitting follows the log-sum-exp merge identity: each split

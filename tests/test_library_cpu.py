@@ -81,3 +81,13 @@ def test_validation_codes(lib, kw, code):
 def test_empty_problems_are_ok_without_a_device(lib):
     assert call(lib, batch=0) == fa.FA_OK
     assert call(lib, sq=0) == fa.FA_OK
+
+
+def test_gqa_validation(lib):
+    def gqa(heads, heads_k):
+        return lib.fa_fwd_gqa(P, P, P, P, P, 1, heads, heads_k, 128, 128, None, None, 0, 0, 128,
+                              128, 0.1, 0, 0, None, None, None, None, 0, None)
+    assert gqa(8, 3) == fa.FA_ERR_INVALID_ARG   # 3 does not divide 8
+    assert gqa(8, 0) == fa.FA_ERR_INVALID_ARG
+    assert gqa(8, 16) == fa.FA_ERR_INVALID_ARG
+    assert b"heads_k" in lib.fa_last_error_detail()

@@ -176,6 +176,36 @@ def test_many_splits(D):
     compare(o, lse, o_ref, lse_ref, what=f"many splits D={D}")
 
 
+@pytest.mark.parametrize("B,H,Hk,Sq,Sk,D,causal", [
+    (2, 8, 2, 300, 513, 128, False),
+    (2, 8, 2, 513, 513, 128, True),
+    (1, 6, 3, 257, 130, 64, True),
+    (1, 16, 1, 128, 3000, 128, False),   # multi-query; splits the key range
+])
+def test_grouped_query_full(B, H, Hk, Sq, Sk, D, causal):
+    x = inputs.make_random(B, H, Sq, Sk, D, seed=90 + H + Hk + Sq, heads_k=Hk)
+    o, lse = run_gpu(x, causal=causal, softmax_scale=D ** -0.5)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=D ** -0.5,
+                                      causal=causal)
+    compare(o, lse, o_ref, lse_ref, what=f"gqa {(B, H, Hk, Sq, Sk, D, causal)}")
+
+
+def test_grouped_query_varlen_and_fp8():
+    x = inputs.make_varlen([40, 300, 0, 129], [40, 300, 5, 200], heads=4, head_dim=128, seed=95,
+                           heads_k=2)
+    o, lse = run_gpu(x, causal=True, softmax_scale=128 ** -0.5)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=128 ** -0.5,
+                                      causal=True, cu_seqlens_q=x["cu_seqlens_q"],
+                                      cu_seqlens_k=x["cu_seqlens_k"])
+    compare(o, lse, o_ref, lse_ref, what="gqa varlen")
+    w = inputs.Workload("fp8_gqa", 2, 4, 200, 300, 128, False, dtype="e4m3", seed=96, heads_k=1)
+    x = inputs.make_inputs(w)
+    o, lse = run_gpu(x, causal=False, softmax_scale=w.softmax_scale)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=w.softmax_scale,
+                                      descale=x["descale"])
+    compare(o, lse, o_ref, lse_ref, dtype="e4m3", what="gqa fp8")
+
+
 def test_zero_keys_fixed_length():
     x = inputs.make_random(2, 2, 130, 0, 128, seed=3)
     o, lse = run_gpu(x, causal=False, softmax_scale=0.1)
