@@ -14,6 +14,8 @@ Workloads (shapes and value distributions of the attention configurations):
   fp8_noncausal_4k    B=4  H=16 S=4096 D=128 e4m3 per-tensor amax/448  non-causal seed 1005
   bf16_shortq_longkv  B=1  H=8  Sq=128 Sk=65536 D=128 N(0,1) non-causal  seed 1006
   bf16_gqa_causal_8k  B=2  H=32 (8 K/V heads) S=8192 D=128 2*N(0,1) causal seed 1007
+  fp8_headscale_4k    B=4  H=16 S=4096 D=128 Q/K e4m3, V e5m2, one descale per
+                      (batch, head) = amax/max-finite       non-causal  seed 1008
 """
 from __future__ import annotations
 
@@ -24,6 +26,8 @@ from typing import Optional
 import torch
 
 E4M3_MAX = 448.0
+E5M2_MAX = 57344.0
+_FP8 = {"e4m3": (torch.float8_e4m3fn, E4M3_MAX), "e5m2": (torch.float8_e5m2, E5M2_MAX)}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -35,7 +39,9 @@ class Workload:
     seqlen_k: int
     head_dim: int
     causal: bool
-    dtype: str = "bf16"          # "bf16" or "e4m3"
+    dtype: str = "bf16"          # "bf16" or "e4m3" (the type of Q and K, and of V by default)
+    v_dtype: str = ""            # "e5m2" to store V as E5M2 (FP8 only); "" = dtype
+    descale: str = "tensor"      # FP8: "tensor" (one descale per tensor) or "head" (per batch, K/V head)
     amp: float = 1.0             # values are amp * N(0,1)
     seed: int = 0
     varlen: bool = False         # lengths drawn per sequence (seqlen_q/k = max 4096)
@@ -67,6 +73,9 @@ WORKLOADS = {
     # grouped-query attention (4 query heads per K/V head) at the 8K causal shape
     "bf16_gqa_causal_8k": Workload("bf16_gqa_causal_8k", 2, 32, 8192, 8192, 128, True, amp=2.0,
                                    seed=1007, heads_k=8),
+    # FP8 with one descale per (batch, head) and an E5M2 V
+    "fp8_headscale_4k": Workload("fp8_headscale_4k", 4, 16, 4096, 4096, 128, False,
+                                 dtype="e4m3", v_dtype="e5m2", descale="head", seed=1008),
 }
 
 
@@ -80,6 +89,23 @@ def quantize_e4m3(x: torch.Tensor):
     descale = amax / E4M3_MAX if amax > 0 else 1.0
     y = (x / descale).clamp_(-E4M3_MAX, E4M3_MAX)
     return y.to(torch.float8_e4m3fn), descale
+
+
+def quantize_fp8_per_head(x: torch.Tensor, fmt: str, heads_k: int):
+    """FP8 quantisation with one descale per (batch, key/value head).
+
+    x: [B, S, H, D] with H a multiple of heads_k; query heads that share a K/V head
+    share a descale (the amax is taken over the whole group).  descale[b, g] =
+    amax / max-finite of the format, x8 = rn(clamp(x / descale)).
+    Returns (x8, descale fp32 [B, heads_k]).
+    """
+    dt, mx = _FP8[fmt]
+    B, S, H, D = x.shape
+    g = x.reshape(B, S, heads_k, H // heads_k, D)
+    amax = g.abs().amax(dim=(1, 3, 4))                        # [B, heads_k]
+    descale = torch.where(amax > 0, amax / mx, torch.ones_like(amax)).to(torch.float32)
+    y = (g / descale.view(B, 1, heads_k, 1, 1)).clamp_(-mx, mx).reshape(B, S, H, D)
+    return y.to(dt), descale
 
 
 def varlen_lengths(w: Workload, gen: torch.Generator):
@@ -105,7 +131,8 @@ def varlen_lengths(w: Workload, gen: torch.Generator):
 def make_inputs(w: Workload, *, seed: Optional[int] = None, shapes_only_q: Optional[int] = None):
     """Draw (on the CPU) the inputs of a workload.
 
-    Returns a dict with q, k, v (bf16 or float8_e4m3fn, CPU), descale (q, k, v),
+    Returns a dict with q, k, v (bf16 or float8, CPU), descale (q, k, v: python
+    floats, or fp32 [B, Hk] tensors for per-head descales),
     cu_seqlens_q/k (int32 CPU tensors or None), max_seqlen_q/k, seqlens.
     Draw order: Q, K, V (fp32 N(0,1), times amp), then varlen lengths.
     For varlen, the lengths are drawn first from their own generator stream
@@ -135,7 +162,16 @@ def make_inputs(w: Workload, *, seed: Optional[int] = None, shapes_only_q: Optio
         q.mul_(w.amp)
         k.mul_(w.amp)
         v.mul_(w.amp)
-    if w.dtype == "e4m3":
+    if w.dtype == "e4m3" and w.descale == "head":
+        if w.varlen:
+            raise ValueError("per-head descales are drawn for fixed-length workloads only")
+        q, dq = quantize_fp8_per_head(q, "e4m3", w.kv_heads)
+        k, dk = quantize_fp8_per_head(k, "e4m3", w.kv_heads)
+        v, dv = quantize_fp8_per_head(v, w.v_dtype or "e4m3", w.kv_heads)
+        descale = (dq, dk, dv)
+    elif w.dtype == "e4m3":
+        if w.v_dtype not in ("", "e4m3"):
+            raise ValueError("a per-tensor E5M2 V is not drawn; use descale='head'")
         q8, dq = quantize_e4m3(q)
         k8, dk = quantize_e4m3(k)
         v8, dv = quantize_e4m3(v)
@@ -148,10 +184,10 @@ def make_inputs(w: Workload, *, seed: Optional[int] = None, shapes_only_q: Optio
 
 
 def make_random(batch, heads, seqlen_q, seqlen_k, head_dim, *, seed, amp=1.0,
-                dtype="bf16", heads_k=0):
+                dtype="bf16", heads_k=0, v_dtype="", descale="tensor"):
     """Fixed-length N(0,1)*amp inputs of an arbitrary shape (for edge cases)."""
     w = Workload("custom", batch, heads, seqlen_q, seqlen_k, head_dim, False, dtype=dtype,
-                 amp=amp, seed=seed, heads_k=heads_k)
+                 amp=amp, seed=seed, heads_k=heads_k, v_dtype=v_dtype, descale=descale)
     return make_inputs(w)
 
 

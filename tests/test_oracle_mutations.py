@@ -3,7 +3,8 @@
 Each case plants one mistake in a copy of oracle/attn_oracle.c -- a dropped
 scale, a wrong sign, an off-by-one in the causal mask, the other diagonal
 alignment, a base-2 LSE, a transposed or mis-strided operand, a decoder slip,
-a missing descale, a NaN for empty rows -- builds it, and runs the pin suite
+a missing or mis-indexed descale, a NaN for empty rows, an ignored per-sequence
+key length, an append one row off -- builds it, and runs the pin suite
 (tests/test_oracle_pins.py) against that build.  Every mutant must be rejected
 by at least one pin; the unmodified source must pass.
 """
@@ -35,10 +36,21 @@ MUTANTS = {
     "gqa_k_uses_query_head": ("int64_t k_off = ((k_row0 + j) * heads_k + hk) * (int64_t)d;",
                               "int64_t k_off = ((k_row0 + j) * heads_k + h % heads_k) * (int64_t)d;"),
     "q_row_ignores_batch": ("q_row = b * (int64_t)seqlen_q + i;", "q_row = i;"),
-    "v_uses_k": ("o_row[c] += p * (orc_load(v, dtype, v_off + c) * v_descale);",
-                 "o_row[c] += p * (orc_load(k, dtype, v_off + c) * v_descale);"),
-    "k_descale_missing": ("(orc_load(k, dtype, k_off + c) * k_descale);", "(orc_load(k, dtype, k_off + c));"),
-    "v_descale_missing": ("(orc_load(v, dtype, v_off + c) * v_descale);", "(orc_load(v, dtype, v_off + c));"),
+    "v_uses_k": ("o_row[c] += p * (orc_load(v, v_dtype, v_off + c) * vd);",
+                 "o_row[c] += p * (orc_load(k, v_dtype, v_off + c) * vd);"),
+    "k_descale_missing": ("(orc_load(k, k_dtype, k_off + c) * kd);", "(orc_load(k, k_dtype, k_off + c));"),
+    "v_descale_missing": ("(orc_load(v, v_dtype, v_off + c) * vd);", "(orc_load(v, v_dtype, v_off + c));"),
+    "v_decoded_as_k_type": ("orc_load(v, v_dtype, v_off + c)", "orc_load(v, k_dtype, v_off + c)"),
+    "descale_per_query_head": ("const int64_t ds = b * descale_stride_b + hk * descale_stride_h;",
+                               "const int64_t ds = b * descale_stride_b + (h % heads_k) * descale_stride_h;"),
+    "descale_ignores_batch": ("const int64_t ds = b * descale_stride_b + hk * descale_stride_h;",
+                              "const int64_t ds = hk * descale_stride_h;"),
+    "v_descale_from_k": ("const double vd = v_descale ? v_descale[ds] : 1.0;",
+                         "const double vd = k_descale ? k_descale[ds] : 1.0;"),
+    "e5m2_bias": ("ldexp(1.0 + (double)m / 4.0, e - 15)", "ldexp(1.0 + (double)m / 4.0, e - 16)"),
+    "e5m2_subnormal": ("ldexp((double)m / 4.0, -14)", "ldexp((double)m / 4.0, -15)"),
+    "seqused_k_ignored": ("        if (seqused_k) sk = seqused_k[b];\n", ""),
+    "append_one_row_late": ("seqlens[b] + i) * row_bytes", "seqlens[b] + i + 1) * row_bytes"),
     "empty_rows_nan": ("            lse_out[r] = -INFINITY;\n            continue;",
                        "            lse_out[r] = NAN;\n            continue;"),
     "e4m3_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),

@@ -358,3 +358,115 @@ def test_grouped_query_rejects_indivisible_heads():
     k = np.zeros((1, 2, 2, 4))
     with pytest.raises(ValueError):
         oracle.attention(q, k, k, softmax_scale=1.0)
+
+
+# --------------------------------------------------------------------------
+# FP8 with per-(batch, head) descales and an E5M2 V; per-sequence key
+# lengths inside a fixed-capacity cache; appending new keys to that cache
+# --------------------------------------------------------------------------
+def test_e5m2_decoder_matches_fp16_bits_and_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    # an E5M2 code is the high byte of an IEEE binary16 of the same value
+    half = (codes.astype(np.uint16) << 8).view(np.float16).astype(np.float64)
+    tvals = torch.from_numpy(codes).view(torch.float8_e5m2).to(torch.float64).numpy()
+    got = oracle.decode(codes, oracle.DT_E5M2)
+    nan = np.isnan(half)
+    assert np.array_equal(nan, np.isnan(got)) and np.array_equal(nan, np.isnan(tvals))
+    assert np.array_equal(got[~nan], half[~nan]) and np.array_equal(got[~nan], tvals[~nan])
+    assert got[0x7B] == 57344.0 and got[0x01] == 2.0 ** -16 and got[0x7C] == np.inf
+    assert got[0xFC] == -np.inf and got[0x04] == 2.0 ** -14
+
+
+@pytest.mark.parametrize("H, Hk, causal", [(4, 4, False), (4, 2, True), (3, 1, True)])
+def test_per_head_descale_equals_dequantised_fp64(H, Hk, causal):
+    from exact_attention_forward_gb300 import inputs
+    g = torch.Generator().manual_seed(40 + H + Hk)
+    B, Sq, Sk, D = 3, 9, 13, 8
+    # per-head amplitudes differ so that a descale read from the wrong (b, head) shows
+    amp_q = torch.rand((B, 1, H, 1), generator=g) * 3 + 0.2
+    amp_k = torch.rand((B, 1, Hk, 1), generator=g) * 3 + 0.2
+    q = torch.randn((B, Sq, H, D), generator=g) * amp_q
+    k = torch.randn((B, Sk, Hk, D), generator=g) * amp_k
+    v = torch.randn((B, Sk, Hk, D), generator=g) * amp_k
+    q8, dq = inputs.quantize_fp8_per_head(q, "e4m3", Hk)
+    k8, dk = inputs.quantize_fp8_per_head(k, "e4m3", Hk)
+    v8, dv = inputs.quantize_fp8_per_head(v, "e5m2", Hk)
+    assert q8.dtype == torch.float8_e4m3fn and v8.dtype == torch.float8_e5m2
+    o, lse = oracle.attention(q8, k8, v8, softmax_scale=0.3, causal=causal, descale=(dq, dk, dv))
+    # dequantise with torch's own FP8 decoders: each (b, head) slice times its descale
+    grp = H // Hk
+    d64 = lambda t: t.to(torch.float64)
+    deq_q = d64(q8) * d64(dq).repeat_interleave(grp, dim=1)[:, None, :, None]
+    deq_k = d64(k8) * d64(dk)[:, None, :, None]
+    deq_v = d64(v8) * d64(dv)[:, None, :, None]
+    o2, lse2 = oracle.attention(deq_q, deq_k, deq_v, softmax_scale=0.3, causal=causal)
+    assert np.allclose(o, o2, rtol=0, atol=1e-12) and np.allclose(lse, lse2, rtol=0, atol=1e-12)
+    O, L = brute_force(deq_q.numpy().tolist(), deq_k.numpy().tolist(), deq_v.numpy().tolist(),
+                       0.3, causal)
+    assert np.allclose(o, np.array(O), rtol=0, atol=1e-10)
+    assert np.allclose(lse, np.array(L), rtol=0, atol=1e-10)
+    # a scalar descale is the same as a constant per-head array
+    o3, lse3 = oracle.attention(q8, k8, v8, softmax_scale=0.3, causal=causal,
+                                descale=(0.5, 0.25, 2.0))
+    o4, lse4 = oracle.attention(q8, k8, v8, softmax_scale=0.3, causal=causal,
+                                descale=(np.full((B, Hk), 0.5), np.full((B, Hk), 0.25),
+                                         np.full((B, Hk), 2.0)))
+    assert np.array_equal(o3, o4) and np.array_equal(lse3, lse4)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_seqused_k_equals_truncated_keys(causal):
+    rng = np.random.default_rng(41)
+    B, Sq, cap, H, Hk, D = 4, 5, 11, 2, 1, 4
+    used = [11, 0, 6, 3]          # full, empty, partial, shorter than Sq
+    q, k, v = _rand((B, Sq, H, D), rng), _rand((B, cap, Hk, D), rng), _rand((B, cap, Hk, D), rng)
+    o, lse = oracle.attention(q, k, v, softmax_scale=0.7, causal=causal, seqused_k=used)
+    for b in range(B):
+        u = used[b]
+        if u == 0:
+            assert np.all(o[b] == 0) and np.all(lse[b] == -np.inf)
+            continue
+        O, L = brute_force(q[b:b + 1].tolist(), k[b:b + 1, :u].tolist(), v[b:b + 1, :u].tolist(),
+                           0.7, causal)
+        L = np.array(L)[0]
+        fin = np.isfinite(L)
+        assert np.array_equal(fin, np.isfinite(lse[b]))
+        assert np.allclose(lse[b][fin], L[fin], rtol=0, atol=1e-12)
+        O = np.array([[row if row is not None else [0.0] * D for row in r] for r in O[0]])
+        assert np.allclose(o[b], O, rtol=0, atol=1e-12)
+    with pytest.raises(ValueError):  # more keys used than stored
+        oracle.attention(q, k, v, softmax_scale=0.7, seqused_k=[12, 0, 0, 0])
+
+
+def test_append_kv_writes_rows_and_attention_sees_them():
+    g = torch.Generator().manual_seed(42)
+    B, cap, Hk, H, D, n_new = 3, 12, 2, 4, 8, 4
+    seqlens = [3, 0, 8]
+    cache = torch.randn((B, cap, Hk, D), generator=g).to(torch.bfloat16)
+    new = torch.randn((B, n_new, Hk, D), generator=g).to(torch.bfloat16)
+    before = cache.clone()
+    out = oracle.append_kv(cache, new, seqlens)
+    assert out.dtype == torch.bfloat16 and torch.equal(cache, before)  # input untouched
+    for b, s in enumerate(seqlens):
+        assert torch.equal(out[b, :s], cache[b, :s])
+        assert torch.equal(out[b, s:s + n_new], new[b])
+        assert torch.equal(out[b, s + n_new:], cache[b, s + n_new:])
+    with pytest.raises(ValueError):
+        oracle.append_kv(cache, new, [3, 0, 9])  # 9 + 4 > capacity
+    # attention of the new queries over the grown cache == torch SDPA (fp64, explicit
+    # bottom-right causal mask) over the concatenation of old prefix and new keys
+    vcache = torch.randn((B, cap, Hk, D), generator=g).to(torch.bfloat16)
+    vnew = torch.randn((B, n_new, Hk, D), generator=g).to(torch.bfloat16)
+    kc, vc = out, oracle.append_kv(vcache, vnew, seqlens)
+    q = torch.randn((B, n_new, H, D), generator=g).to(torch.bfloat16)
+    used = [s + n_new for s in seqlens]
+    o, lse = oracle.attention(q, kc, vc, softmax_scale=0.35, causal=True, seqused_k=used)
+    for b, s in enumerate(seqlens):
+        kk = torch.cat([cache[b, :s], new[b]]).to(torch.float64).repeat_interleave(H // Hk, dim=1)
+        vv = torch.cat([vcache[b, :s], vnew[b]]).to(torch.float64).repeat_interleave(H // Hk, dim=1)
+        qq = q[b].to(torch.float64)
+        sk = s + n_new
+        mask = torch.arange(sk)[None, :] <= torch.arange(n_new)[:, None] + (sk - n_new)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qq.transpose(0, 1), kk.transpose(0, 1), vv.transpose(0, 1), attn_mask=mask, scale=0.35)
+        assert np.allclose(o[b], ref.transpose(0, 1).numpy(), rtol=0, atol=1e-12)
