@@ -35,8 +35,21 @@ DEFAULT_WORKLOAD = "bf16_causal_8k"
 L2_FLUSH_BYTES = 256 << 20
 
 
+def _cache_used(w, x):
+    """Cache workloads: keys each sequence attends over (filled length + new rows)."""
+    return [int(n) + w.cache_new for n in x["cache_seqlens"].tolist()]
+
+
 def _flops(w, x) -> float:
-    """Algorithmic FLOPs of one pass: 4 * Sq * Sk * D per (batch, head), halved when causal."""
+    """Algorithmic FLOPs of one pass: 4 * Sq * Sk * D per (batch, head), halved when causal
+    (cache workloads: 4 * D per visible (query row, key) pair, bottom-right causal)."""
+    if w.cache_new:
+        tot = 0.0
+        for used in _cache_used(w, x):
+            for i in range(w.seqlen_q):
+                vis = min(used, used - w.seqlen_q + i + 1) if w.causal else used
+                tot += 4.0 * w.heads * w.head_dim * max(vis, 0)
+        return tot
     if w.varlen:
         sq, sk = x["seqlens"]
         tot = sum(4.0 * w.heads * a * b * w.head_dim for a, b in zip(sq, sk))
@@ -45,11 +58,19 @@ def _flops(w, x) -> float:
     return tot / 2 if w.causal else tot
 
 
-def _bytes(x) -> float:
-    """Compulsory HBM bytes of one pass: Q, K, V read once; O (bf16) and LSE (fp32) written."""
+def _bytes(w, x) -> float:
+    """Compulsory HBM bytes of one pass: Q, K, V read once; O (bf16) and LSE (fp32) written.
+    Cache workloads: the filled cache rows each sequence uses are read once, the new rows
+    are read once and written into the cache once."""
     q, k, v = x["q"], x["k"], x["v"]
     rows = q.numel() // q.shape[-1]  # query rows x heads = LSE entries
-    return (q.numel() + k.numel() + v.numel()) * q.element_size() + rows * v.shape[-1] * 2 + rows * 4
+    out = rows * v.shape[-1] * 2 + rows * 4 + q.numel() * q.element_size()
+    if w.cache_new:
+        row_kv = k.shape[2] * k.shape[3] * k.element_size()  # one cache row of one tensor
+        used = sum(_cache_used(w, x))
+        new = x["k_new"].numel() * x["k_new"].element_size()
+        return out + 2 * used * row_kv + 2 * 2 * new
+    return out + (k.numel() + v.numel()) * q.element_size()
 
 
 def _source_sha() -> str:
@@ -182,16 +203,30 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle (baseline)
-def _oracle_rows_flops(w, rows):
+def _oracle_rows_flops(w, rows, used=None):
     sq, sk = w.seqlen_q, w.seqlen_k
     tot = 0.0
-    for _, _, i in rows:
+    for b, _, i in rows:
+        if used is not None:
+            sk = used[b]
         n = sk if not w.causal else max(0, min(sk, i + sk - sq + 1))
         tot += 4.0 * n * w.head_dim
     return tot
 
 
-def _oracle_sample(w, x, budget_s: float, seed: int = 0):
+def _oracle_inputs(w, x):
+    """What the oracle attends over: for cache workloads, the caches with the new rows
+    appended (by the oracle's own append) and the per-sequence lengths."""
+    if not w.cache_new:
+        return dict(q=x["q"], k=x["k"], v=x["v"], descale=x["descale"], seqused_k=None)
+    import oracle
+    lens = x["cache_seqlens"].tolist()
+    return dict(q=x["q"], k=oracle.append_kv(x["k"], x["k_new"], lens),
+                v=oracle.append_kv(x["v"], x["v_new"], lens), descale=x["descale"],
+                seqused_k=_cache_used(w, x))
+
+
+def _oracle_sample(w, xo, budget_s: float, seed: int = 0):
     """Time the oracle on seeded random rows of the workload until ~budget_s of CPU work."""
     import numpy as np
     import oracle
@@ -202,11 +237,11 @@ def _oracle_sample(w, x, budget_s: float, seed: int = 0):
         rows = np.stack([rng.integers(0, w.batch, n), rng.integers(0, w.heads, n),
                          rng.integers(0, w.seqlen_q, n)], axis=1).astype(np.int64)
         t0 = time.perf_counter()
-        oracle.attention_rows(x["q"], x["k"], x["v"], rows, softmax_scale=w.softmax_scale,
-                              causal=w.causal, descale=x["descale"])
+        oracle.attention_rows(xo["q"], xo["k"], xo["v"], rows, softmax_scale=w.softmax_scale,
+                              causal=w.causal, descale=xo["descale"], seqused_k=xo["seqused_k"])
         dt = time.perf_counter() - t0
         if dt >= budget_s or n >= w.batch * w.heads * w.seqlen_q:
-            return _oracle_rows_flops(w, rows), dt, n
+            return _oracle_rows_flops(w, rows, xo["seqused_k"]), dt, n
         grow = max(2.0, min(16.0, budget_s / max(dt, 1e-3)))
         n = int(n * grow)
 
@@ -224,13 +259,14 @@ def run_reference(args, w):
     os.environ.setdefault("OMP_NUM_THREADS", str(_oracle_threads()))
     from exact_attention_forward_gb300 import inputs
     x = inputs.make_inputs(w)
+    xo = _oracle_inputs(w, x)
     per_step = max(2.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        _oracle_sample(w, x, per_step / 4, seed=1)
+        _oracle_sample(w, xo, per_step / 4, seed=1)
     flops = secs = 0.0
     rows_total = 0
     for s in range(args.steps):
-        f, dt, n = _oracle_sample(w, x, per_step, seed=100 + s)
+        f, dt, n = _oracle_sample(w, xo, per_step, seed=100 + s)
         flops += f
         secs += dt
         rows_total += n
@@ -259,6 +295,13 @@ def _config(w, l2):
          "input_dtype": w.dtype, "values": f"{w.amp:g}*N(0,1) seed {w.seed}", "l2": l2}
     if w.varlen:
         c["varlen"] = f"{w.n_seqs} seqs U{{1..{w.seqlen_q}}} + {len(w.empty_k_at)} with Sk=0"
+    if w.cache_new:
+        c["kv_cache"] = (f"capacity {w.seqlen_k}, filled U{{{w.seqlen_k // 2}.."
+                         f"{w.seqlen_k - w.cache_new}}}, {w.cache_new} new row(s) appended per step")
+    if w.v_dtype:
+        c["v_dtype"] = w.v_dtype
+    if w.descale != "tensor":
+        c["descale"] = "per (batch, K/V head)"
     return c
 
 
@@ -284,7 +327,11 @@ def run_gpu(args, w):
     cu_q = x["cu_seqlens_q"].to(dev) if w.varlen else None
     cu_k = x["cu_seqlens_k"].to(dev) if w.varlen else None
     fp8 = w.dtype == "e4m3"
-    descale = [torch.tensor(d, dtype=torch.float32, device=dev) for d in x["descale"]] if fp8 else None
+    descale = ([torch.as_tensor(d, dtype=torch.float32).to(dev) for d in x["descale"]]
+               if fp8 else None)
+    cache = None
+    if w.cache_new:
+        cache = {n: x[n].to(dev) for n in ("k_new", "v_new", "cache_seqlens")}
     o_shape = (q.shape[0], q.shape[1], q.shape[2], v.shape[-1]) if not w.varlen else \
         (q.shape[0], q.shape[1], v.shape[-1])
     o = torch.empty(o_shape, dtype=torch.bfloat16, device=dev)
@@ -307,6 +354,11 @@ def run_gpu(args, w):
         flush_rd.max()
 
     def step():
+        if cache is not None:  # append the new rows (same rows, same place: idempotent), attend
+            fa.fwd_kvcache(q, k, v, cache["cache_seqlens"], cache["k_new"], cache["v_new"],
+                           causal=w.causal, softmax_scale=w.softmax_scale, descale=descale,
+                           workspace=ws, out=o, lse=lse, stream=stream)
+            return
         fa.fwd(q, k, v, causal=w.causal, softmax_scale=w.softmax_scale, cu_seqlens_q=cu_q,
                cu_seqlens_k=cu_k, max_seqlen_q=x["max_seqlen_q"], max_seqlen_k=x["max_seqlen_k"],
                descale=descale, workspace=ws, out=o, lse=lse, stream=stream)
@@ -345,19 +397,29 @@ def run_gpu(args, w):
     # ---------------- end to end through the public API, host buffers
     e2e = None
     if not args.skip_e2e:
-        hq, hk, hv = (t.cpu().pin_memory() for t in (x["q"], x["k"], x["v"]))
+        # per step, the inputs come from pinned host memory: Q, K, V -- or, for a cache
+        # workload, Q, the new K/V rows and the cache lengths (the cache itself is state
+        # that lives on the device)
+        names = ("q", "k_new", "v_new", "cache_seqlens") if cache is not None else ("q", "k", "v")
+        host = {n: x[n].cpu().contiguous().pin_memory() for n in names}
+        devb = {n: torch.empty_like(host[n], device=dev) for n in names}
         ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        dq, dk, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
 
         def e2e_step():
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv_.copy_(hv, non_blocking=True)
-            oo, ll = fa.fwd(dq, dk, dv_, causal=w.causal, softmax_scale=w.softmax_scale,
-                            cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=x["max_seqlen_q"],
-                            max_seqlen_k=x["max_seqlen_k"], descale=descale, workspace=ws,
-                            out=o, lse=lse, stream=stream)
+            for n in names:
+                devb[n].copy_(host[n], non_blocking=True)
+            if cache is not None:
+                oo, ll = fa.fwd_kvcache(devb["q"], k, v, devb["cache_seqlens"], devb["k_new"],
+                                        devb["v_new"], causal=w.causal,
+                                        softmax_scale=w.softmax_scale, descale=descale,
+                                        workspace=ws, out=o, lse=lse, stream=stream)
+            else:
+                oo, ll = fa.fwd(devb["q"], devb["k"], devb["v"], causal=w.causal,
+                                softmax_scale=w.softmax_scale, cu_seqlens_q=cu_q,
+                                cu_seqlens_k=cu_k, max_seqlen_q=x["max_seqlen_q"],
+                                max_seqlen_k=x["max_seqlen_k"], descale=descale, workspace=ws,
+                                out=o, lse=lse, stream=stream)
             ho.copy_(oo, non_blocking=True)
             hl.copy_(ll, non_blocking=True)
 
@@ -375,7 +437,7 @@ def run_gpu(args, w):
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
         e2e = {"value": job_throughput(flops, world, n_e2e, e2e_ms) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -393,9 +455,9 @@ def run_gpu(args, w):
         except Exception as exc:  # keep the line; fall back to the nominal ratio
             print(f"fp8 GEMM peak not measured: {exc}", file=sys.stderr)
     kernel_ms = ms_per_step
-    if w.seqlen_q <= 256 and not w.varlen and not w.causal and splits > 1:
+    if w.cache_new or (w.seqlen_q <= 256 and not w.varlen and not w.causal and splits > 1):
         bound, unit = "hbm", "GB/s"
-        achieved = _bytes(x) / (kernel_ms * 1e-3) / 1e9
+        achieved = _bytes(w, x) / (kernel_ms * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
     else:
         bound, unit = "tensor", "TFLOP/s"
@@ -419,7 +481,7 @@ def run_gpu(args, w):
         "dtype": "bf16" if not fp8 else "e4m3", "data": "synthetic",
         "config": _config(w, "flushed between timed steps (256 MiB write + 256 MiB read, untimed)"),
         "clocks": clocks, "e2e": e2e,
-        "gpu_launches": args.steps * (2 if splits > 1 else 1),
+        "gpu_launches": args.steps * ((2 if splits > 1 else 1) + (1 if cache is not None else 0)),
         "roofline": roofline,
         "step_ms": {"min": min(times_ms), "median": statistics.median(times_ms),
                     "max": max(times_ms)},
@@ -427,7 +489,7 @@ def run_gpu(args, w):
     }
     if rank == 0 and not args.skip_cpu_baseline and world == 1:
         os.environ.setdefault("OMP_NUM_THREADS", str(_oracle_threads()))
-        f, dt, n = _oracle_sample(w, x, args.cpu_seconds)
+        f, dt, n = _oracle_sample(w, _oracle_inputs(w, x), args.cpu_seconds)
         line["cpu_baseline"] = {"value": f / dt / 1e12, "unit": "TFLOP/s",
                                 "cores": _oracle_threads(), "kind": "oracle",
                                 "sample": f"{n} seeded random query rows of {w.name} "

@@ -9,10 +9,17 @@ it raises.
 
     o, lse = fwd(q, k, v, causal=True)
 
-q, k, v: CUDA tensors, bf16 or float8_e4m3fn, [B, S, H, D] (or packed
-[total, H, D] with cu_seqlens_q / cu_seqlens_k int32 [B + 1] on the device);
-k and v may have fewer heads than q (grouped-query attention).
-Returns o (bf16, q's layout) and lse (fp32, [B, H, Sq] or [H, total_q]).
+q, k, v: CUDA tensors, bf16 or float8_e4m3fn (v may be float8_e5m2 with
+e4m3 q/k), [B, S, H, D] (or packed [total, H, D] with cu_seqlens_q /
+cu_seqlens_k int32 [B + 1] on the device); k and v may have fewer heads than
+q (grouped-query attention).  FP8 descales are scalars or one value per
+(batch, K/V head).  Returns o (bf16, q's layout) and lse (fp32, [B, H, Sq] or
+[H, total_q]).
+
+    o, lse = fwd_kvcache(q, k_cache, v_cache, cache_seqlens, k_new, v_new, causal=True)
+
+appends k_new / v_new to the caches at cache_seqlens and attends over the
+first cache_seqlens + seqlen_new rows of each sequence.
 """
 from __future__ import annotations
 
@@ -21,20 +28,20 @@ import math
 import os
 import threading
 
-__all__ = ["fwd", "fa_fwd", "FaError", "workspace_size", "num_splits", "device_error",
-           "debug_set", "library_path", "EXPORTED_SYMBOLS", "load_library"]
+__all__ = ["fwd", "fwd_kvcache", "fa_fwd", "FaError", "workspace_size", "num_splits",
+           "device_error", "debug_set", "library_path", "EXPORTED_SYMBOLS", "load_library"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_fa_gb300.so")
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_WORKSPACE, \
-    FA_ERR_DEVICE_TIMEOUT = range(6)
-FA_DTYPE_BF16, FA_DTYPE_E4M3 = 0, 1
+    FA_ERR_DEVICE_TIMEOUT, FA_ERR_DEVICE_ARG = range(7)
+FA_DTYPE_BF16, FA_DTYPE_E4M3, FA_DTYPE_E5M2 = 0, 1, 2
 
 # Every function declared in include/fa.h.
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_num_splits", "fa_status_string",
                     "fa_last_error_detail", "fa_device_error", "fa_debug_set",
-                    "fa_fwd_static_workspace", "fa_fwd_gqa")
+                    "fa_fwd_static_workspace", "fa_fwd_gqa", "fa_fwd_fp8", "fa_fwd_kvcache")
 
 _lock = threading.Lock()
 _lib = None
@@ -81,6 +88,14 @@ def load_library():
         lib.fa_fwd_gqa.restype = i32
         lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, i32,
                                    i32, i32, f32, i32, i32, vp, vp, vp, vp, sz, vp]
+        i64 = ctypes.c_int64
+        lib.fa_fwd_fp8.restype = i32
+        lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, i32,
+                                   i32, f32, i32, i32, vp, vp, vp, i64, i64, vp, sz, vp]
+        lib.fa_fwd_kvcache.restype = i32
+        lib.fa_fwd_kvcache.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp,
+                                       i32, i32, f32, i32, i32, i32, vp, vp, vp, i64, i64, vp, sz,
+                                       vp]
         lib.fa_fwd_static_workspace.restype = i32
         lib.fa_fwd_static_workspace.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                                 f32, i32, i32, vp, vp, vp, vp]
@@ -124,15 +139,48 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+def _fp8_descales(descale, batch, heads_k, dev, temps):
+    """(q, k, v) descales -> three fp32 CUDA tensors (or None) and the (batch, head)
+    strides of the C ABI: all scalars -> 0-d tensors, strides (0, 0); otherwise every
+    descale becomes a contiguous [batch, heads_k] tensor, strides (heads_k, 1)."""
+    import torch
+
+    if descale is None:
+        return [None, None, None], 0, 0
+    per_head = any(isinstance(x, torch.Tensor) and x.numel() > 1 for x in descale)
+    out = []
+    for x in descale:
+        if x is None and not per_head:
+            out.append(None)
+            continue
+        if x is None:
+            x = 1.0
+        if not isinstance(x, torch.Tensor):
+            x = torch.tensor(float(x), dtype=torch.float32, device=dev)
+            temps.append(x)
+        if per_head:
+            y = x.to(device=dev, dtype=torch.float32).expand(batch, heads_k).contiguous()
+            if y is not x:
+                temps.append(y)
+            x = y
+        elif x.dtype != torch.float32 or x.device != dev:  # one value: move it over
+            x = x.to(device=dev, dtype=torch.float32).reshape(())
+            temps.append(x)
+        out.append(x)
+    return out, (heads_k if per_head else 0), (1 if per_head else 0)
+
+
 def fwd(q, k, v, *, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seqlens_k=None,
         max_seqlen_q=None, max_seqlen_k=None, descale=None, workspace="auto", out=None,
         lse=None, stream=None):
     """Attention forward on the current CUDA device.  Returns (o, lse).
 
-    descale: for float8_e4m3fn inputs, (q, k, v) descales as python floats or
-    0-d fp32 CUDA tensors (None = 1.0).  workspace: "auto" (allocated with
-    torch when the shape benefits from splitting the key range), None (never
-    split) or a caller-owned uint8 CUDA tensor.
+    descale: for FP8 inputs, (q, k, v) descales as python floats, 0-d fp32 CUDA
+    tensors, or fp32 CUDA tensors of shape [B, Hk] (one value per batch and K/V
+    head) (None = 1.0).  v may be float8_e5m2 when q and k are float8_e4m3fn.
+    workspace: "auto" (allocated with torch when the shape benefits from
+    splitting the key range), None (never split) or a caller-owned uint8 CUDA
+    tensor.
     """
     import torch
 
@@ -148,8 +196,9 @@ def fwd(q, k, v, *, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
         dt = FA_DTYPE_E4M3
     else:
         raise ValueError(f"unsupported dtype {q.dtype}")
-    if k.dtype != q.dtype or v.dtype != q.dtype:
-        raise ValueError("q, k, v must share one dtype")
+    v_e5m2 = dt == FA_DTYPE_E4M3 and v.dtype == torch.float8_e5m2
+    if k.dtype != q.dtype or (v.dtype != q.dtype and not v_e5m2):
+        raise ValueError("q, k, v must share one dtype (or be e4m3, e4m3, e5m2)")
     varlen = cu_seqlens_q is not None
     heads_k = k.shape[-2]
     if varlen:
@@ -179,15 +228,10 @@ def fwd(q, k, v, *, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
     if lse is None:
         lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
     ds = [None, None, None]
+    ds_b = ds_h = 0
     temps = []  # tensors made here that must outlive the kernel on `stream`
-    if dt == FA_DTYPE_E4M3 and descale is not None:
-        for i, x in enumerate(descale):
-            if x is None:
-                continue
-            if not isinstance(x, torch.Tensor):
-                x = torch.tensor(float(x), dtype=torch.float32, device=dev)
-                temps.append(x)
-            ds[i] = x
+    if dt == FA_DTYPE_E4M3:
+        ds, ds_b, ds_h = _fp8_descales(descale, batch, heads_k, dev, temps)
     ws = None
     ws_bytes = 0
     if isinstance(workspace, str):
@@ -204,11 +248,89 @@ def fwd(q, k, v, *, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
         ws_bytes = workspace.numel() * workspace.element_size()
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    st = lib.fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(batch), int(heads),
-                    int(heads_k), int(sq_arg), int(sk_arg), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), mq, mk,
-                    int(d), int(dv), float(softmax_scale), int(bool(causal)), dt,
-                    _ptr(ds[0]), _ptr(ds[1]), _ptr(ds[2]), _ptr(ws), ws_bytes,
-                    ctypes.c_void_p(stream.cuda_stream))
+    if dt == FA_DTYPE_E4M3 and (v_e5m2 or ds_b or ds_h):
+        if d != dv:
+            raise ValueError("FP8 needs head_dim == head_dim_v")
+        st = lib.fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(batch),
+                            int(heads), int(heads_k), int(sq_arg), int(sk_arg),
+                            _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), mq, mk, int(d),
+                            float(softmax_scale), int(bool(causal)),
+                            FA_DTYPE_E5M2 if v_e5m2 else FA_DTYPE_E4M3,
+                            _ptr(ds[0]), _ptr(ds[1]), _ptr(ds[2]), ds_b, ds_h, _ptr(ws), ws_bytes,
+                            ctypes.c_void_p(stream.cuda_stream))
+    else:
+        st = lib.fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(batch),
+                            int(heads), int(heads_k), int(sq_arg), int(sk_arg), _ptr(cu_seqlens_q),
+                            _ptr(cu_seqlens_k), mq, mk, int(d), int(dv), float(softmax_scale),
+                            int(bool(causal)), dt, _ptr(ds[0]), _ptr(ds[1]), _ptr(ds[2]), _ptr(ws),
+                            ws_bytes, ctypes.c_void_p(stream.cuda_stream))
+    if st != FA_OK:
+        raise FaError(st, _detail(lib))
+    for t in temps:
+        t.record_stream(stream)
+    return out, lse
+
+
+def fwd_kvcache(q, k_cache, v_cache, cache_seqlens, k_new=None, v_new=None, *, causal=False,
+                softmax_scale=None, descale=None, workspace="auto", out=None, lse=None,
+                stream=None):
+    """Append k_new / v_new ([B, S_new, Hk, D]) to the caches ([B, capacity, Hk, D],
+    written in place) at rows cache_seqlens[b] (int32 CUDA [B], not modified), then
+    attend q ([B, Sq, H, D]) over the first cache_seqlens[b] + S_new rows of each
+    sequence (causal: bottom-right aligned).  Returns (o [B, Sq, H, D] bf16,
+    lse [B, H, Sq] fp32).  Types and descales as fwd()."""
+    import torch
+
+    lib = load_library()
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("cache_seqlens", cache_seqlens), ("k_new", k_new), ("v_new", v_new)):
+        if t is None:
+            continue
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if cache_seqlens.dtype != torch.int32:
+        raise ValueError("cache_seqlens must be int32")
+    if (k_new is None) != (v_new is None):
+        raise ValueError("give both k_new and v_new, or neither")
+    if q.dtype == torch.bfloat16:
+        dt = vdt = FA_DTYPE_BF16
+    elif q.dtype == torch.float8_e4m3fn:
+        dt = FA_DTYPE_E4M3
+        vdt = FA_DTYPE_E5M2 if v_cache.dtype == torch.float8_e5m2 else FA_DTYPE_E4M3
+    else:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    batch, sq, heads, d = q.shape
+    _, cap, heads_k, _ = k_cache.shape
+    n_new = 0 if k_new is None else k_new.shape[1]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    dev = q.device
+    if out is None:
+        out = torch.empty((batch, sq, heads, d), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((batch, heads, sq), dtype=torch.float32, device=dev)
+    temps = []
+    ds, ds_b, ds_h = ([None, None, None], 0, 0)
+    if dt == FA_DTYPE_E4M3:
+        ds, ds_b, ds_h = _fp8_descales(descale, batch, heads_k, dev, temps)
+    ws, ws_bytes = None, 0
+    if isinstance(workspace, str):
+        need = workspace_size(batch, heads, sq, cap, d, causal) if sq > 0 else 0
+        if need > 0:
+            ws = torch.empty(need, dtype=torch.uint8, device=dev)
+            ws_bytes = need
+            temps.append(ws)
+    elif workspace is not None:
+        ws = workspace
+        ws_bytes = workspace.numel() * workspace.element_size()
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    st = lib.fa_fwd_kvcache(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+                            _ptr(out), _ptr(lse), int(batch), int(heads), int(heads_k), int(sq),
+                            int(cap), _ptr(cache_seqlens), int(n_new), int(d),
+                            float(softmax_scale), int(bool(causal)), dt, vdt, _ptr(ds[0]),
+                            _ptr(ds[1]), _ptr(ds[2]), ds_b, ds_h, _ptr(ws), ws_bytes,
+                            ctypes.c_void_p(stream.cuda_stream))
     if st != FA_OK:
         raise FaError(st, _detail(lib))
     for t in temps:

@@ -230,6 +230,181 @@ cudaError_t launch_combine(const float* ws_o, const float* ws_lse, void* o, floa
                               seqlen_q, n_splits);
 }
 
+// Every entry point fills one of these; fwd_impl validates and launches.
+struct FwdArgs {
+    const void *q, *k, *v;
+    void* o;
+    float* lse;
+    int batch, heads, heads_k, seqlen_q, seqlen_k;
+    const int32_t *cu_q, *cu_k;
+    int max_q, max_k, head_dim, head_dim_v;
+    float scale;
+    int causal;
+    fa_dtype dtype, v_dtype;
+    const float *qd, *kd, *vd;
+    long long ds_b, ds_h;
+    const int32_t* seqused_k;   // key/value cache: filled lengths (device, [batch])
+    int seqused_add;            //   + the rows appended by this call
+    const void *k_new, *v_new;  // rows to append first (n_new of them per sequence)
+    int n_new;
+    void* workspace;
+    size_t workspace_bytes;
+    void* stream;
+};
+
+fa_status fwd_impl(const FwdArgs& a) {
+    // ---------------------------------------------------------------- validation
+    const bool varlen = a.cu_q != nullptr || a.cu_k != nullptr;
+    const bool fp8 = a.dtype == FA_DTYPE_E4M3;
+    // with no key rows at all (fixed length seqlen_k == 0, or varlen total 0) K and V may be NULL
+    const bool no_keys = a.seqlen_k == 0;
+    if (!a.q || !a.o || !a.lse || (!no_keys && (!a.k || !a.v)))
+        return fail(FA_ERR_INVALID_ARG, "q, k, v, o and lse must be non-NULL device pointers");
+    if (!aligned16(a.q) || !aligned16(a.k) || !aligned16(a.v) || !aligned16(a.o) ||
+        !aligned16(a.lse))
+        return fail(FA_ERR_INVALID_ARG, "q, k, v, o and lse must be 16-byte aligned");
+    if (a.batch < 0 || a.heads < 1 || a.seqlen_q < 0 || a.seqlen_k < 0)
+        return fail(FA_ERR_INVALID_ARG, "need batch >= 0, heads >= 1, seqlen_q/k >= 0");
+    if (a.heads_k < 1 || a.heads % a.heads_k != 0)
+        return fail(FA_ERR_INVALID_ARG, "heads_k (%d) must be >= 1 and divide heads (%d)",
+                    a.heads_k, a.heads);
+    if (a.causal != 0 && a.causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
+    if (!(a.scale > 0.0f) || !std::isfinite(a.scale))
+        return fail(FA_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
+    if (fp8 ? (a.v_dtype != FA_DTYPE_E4M3 && a.v_dtype != FA_DTYPE_E5M2)
+            : a.v_dtype != FA_DTYPE_BF16)
+        return fail(FA_ERR_INVALID_ARG, "v dtype %d does not go with q/k dtype %d",
+                    (int)a.v_dtype, (int)a.dtype);
+    if (!fp8 && (a.qd || a.kd || a.vd))
+        return fail(FA_ERR_INVALID_ARG, "descale pointers are only meaningful for FP8 inputs");
+    if ((a.qd && (reinterpret_cast<uintptr_t>(a.qd) & 3u)) ||
+        (a.kd && (reinterpret_cast<uintptr_t>(a.kd) & 3u)) ||
+        (a.vd && (reinterpret_cast<uintptr_t>(a.vd) & 3u)))
+        return fail(FA_ERR_INVALID_ARG, "descale pointers must be 4-byte aligned");
+    if (a.ds_b < 0 || a.ds_h < 0)
+        return fail(FA_ERR_INVALID_ARG, "descale strides must be >= 0");
+    if (varlen && (!a.cu_q || !a.cu_k))
+        return fail(FA_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k must both be given");
+    if (varlen && (a.max_q < 0 || a.max_k < 0))
+        return fail(FA_ERR_INVALID_ARG, "max_seqlen_q/k must be >= 0 for varlen");
+    if (a.head_dim != a.head_dim_v)
+        return fail(FA_ERR_UNSUPPORTED, "head_dim (%d) != head_dim_v (%d) is not built",
+                    a.head_dim, a.head_dim_v);
+    if (!fp8 && a.head_dim != 64 && a.head_dim != 128)
+        return fail(FA_ERR_UNSUPPORTED, "bf16 head_dim %d not built (64, 128)", a.head_dim);
+    if (fp8 && a.head_dim != 128)
+        return fail(FA_ERR_UNSUPPORTED, "fp8 head_dim %d not built (128)", a.head_dim);
+    const long long rows_q = varlen ? a.seqlen_q : (long long)a.batch * a.seqlen_q;
+    const long long rows_k = varlen ? a.seqlen_k : (long long)a.batch * a.seqlen_k;
+    if (rows_q * a.heads * a.head_dim >= (1ll << 40) ||
+        rows_k * a.heads_k * a.head_dim >= (1ll << 40))
+        return fail(FA_ERR_INVALID_ARG, "tensor too large");
+    if (rows_q >= (1ll << 31) || rows_k >= (1ll << 31))
+        return fail(FA_ERR_INVALID_ARG, "row count must fit in int32");
+    const int mq = varlen ? a.max_q : a.seqlen_q;
+    const int mk = varlen ? a.max_k : a.seqlen_k;
+    const bool append = a.n_new > 0;
+    if (a.batch == 0 || ((rows_q == 0 || mq == 0) && !append)) return FA_OK;  // nothing to do
+
+    int dev, sms;
+    uint32_t* err;
+    fa_status st = device_info(&dev, &sms, &err);
+    if (st != FA_OK) return st;
+
+    // ---------------------------------------------------------------- decomposition
+    int splits = 1;
+    if (!varlen && a.workspace && mq > 0) {
+        splits = choose_splits(a.batch, a.heads, a.seqlen_q, a.seqlen_k, a.causal, sms);
+        const size_t need = workspace_bytes_for(splits, a.batch, a.heads, a.seqlen_q, a.head_dim_v);
+        if (a.workspace_bytes < need)
+            return fail(FA_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed",
+                        a.workspace_bytes, need);
+        if (!aligned16(a.workspace))
+            return fail(FA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    }
+    FwdParams p{};
+    p.o = a.o;
+    p.lse = a.lse;
+    p.cu_q = a.cu_q;
+    p.cu_k = a.cu_k;
+    p.q_descale = a.qd;
+    p.k_descale = a.kd;
+    p.v_descale = a.vd;
+    p.descale_sb = a.ds_b;
+    p.descale_sh = a.ds_h;
+    p.seqused_k = a.seqused_k;
+    p.seqused_add = a.seqused_add;
+    p.err = err;
+    p.batch = a.batch;
+    p.heads = a.heads;
+    p.kv_group = a.heads / a.heads_k;
+    p.seqlen_q = mq;
+    p.seqlen_k = mk;
+    p.total_q = varlen ? a.seqlen_q : 0;
+    p.n_mpairs = ceil_div(mq, 256);
+    p.n_splits = splits;
+    const int nblk = ceil_div(mk > 0 ? mk : 1, 128);
+    p.blocks_per_split = splits > 1 ? ceil_div(nblk, splits) : (1 << 29);
+    const long long n_items = (long long)p.n_mpairs * a.batch * a.heads * splits;
+    if (n_items >= (1ll << 31)) return fail(FA_ERR_INVALID_ARG, "too many work items");
+    p.n_items = (int)n_items;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.causal = a.causal;
+    p.varlen = varlen ? 1 : 0;
+    p.split = splits > 1 ? 1 : 0;
+    p.v_e5m2 = a.v_dtype == FA_DTYPE_E5M2 ? 1 : 0;
+    if (p.split) {
+        const size_t rows = (size_t)splits * a.batch * a.heads * a.seqlen_q;
+        p.ws_o = static_cast<float*>(a.workspace);
+        p.ws_lse = p.ws_o + rows * a.head_dim_v;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        p.wait_limit_ns = g_wait_limit_ns;
+        p.inject = g_inject;
+    }
+
+    // ---------------------------------------------------------------- tensor maps
+    CUtensorMap tq, tk, tv;
+    // fixed length: (d, head, seq row, batch); varlen: (d, head, packed row, 1)
+    const int nbat = varlen ? 1 : a.batch;
+    if ((st = encode_map(&tq, a.q, fp8, a.head_dim, a.heads, a.seqlen_q, nbat)) != FA_OK) return st;
+    if (no_keys) {  // no key block is ever loaded; any valid map will do
+        tk = tq;
+        tv = tq;
+    } else {
+        if ((st = encode_map(&tk, a.k, fp8, a.head_dim, a.heads_k, a.seqlen_k, nbat)) != FA_OK)
+            return st;
+        if ((st = encode_map(&tv, a.v, fp8, a.head_dim, a.heads_k, a.seqlen_k, nbat)) != FA_OK)
+            return st;
+    }
+
+    // ---------------------------------------------------------------- launches
+    cudaStream_t s = static_cast<cudaStream_t>(a.stream);
+    cudaError_t e;
+    if (append) {  // the new rows go into the cache first (same stream: ordered before the reads)
+        const long long row_bytes = (long long)a.heads_k * a.head_dim * (fp8 ? 1 : 2);
+        e = launch_append_kv(const_cast<void*>(a.k), const_cast<void*>(a.v), a.k_new, a.v_new,
+                             a.seqused_k, a.batch, a.seqlen_k, a.n_new, row_bytes, err, s);
+        if (e != cudaSuccess) return fail(FA_ERR_CUDA, "append launch: %s", cudaGetErrorString(e));
+    }
+    if (rows_q == 0 || mq == 0) return FA_OK;
+    const int grid = (int)(n_items < sms ? n_items : sms);
+    if (fp8)
+        e = launch_fwd_e4m3_d128(tq, tk, tv, p, grid, s);
+    else if (a.head_dim == 64)
+        e = launch_fwd_bf16_d64(tq, tk, tv, p, grid, s);
+    else
+        e = launch_fwd_bf16_d128(tq, tk, tv, p, grid, s);
+    if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
+    if (p.split) {
+        e = launch_combine(p.ws_o, p.ws_lse, a.o, a.lse, a.batch, a.heads, a.seqlen_q,
+                           a.head_dim_v, splits, s);
+        if (e != cudaSuccess) return fail(FA_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
+    }
+    return FA_OK;
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -244,6 +419,7 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_CUDA: return "CUDA error";
     case FA_ERR_WORKSPACE: return "workspace too small";
     case FA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case FA_ERR_DEVICE_ARG: return "device-resident length out of range";
     }
     return "unknown status";
 }
@@ -274,6 +450,8 @@ fa_status fa_device_error(uint32_t* flags, int clear) {
     if (flags) *flags = w;
     if (w & kErrTimeout)
         return fail(FA_ERR_DEVICE_TIMEOUT, "device wait timed out at site %u", (w >> 8) & 0xFFu);
+    if (w & kErrBadLength)
+        return fail(FA_ERR_DEVICE_ARG, "a cache length was out of range (rows computed with it clamped)");
     return FA_OK;
 }
 
@@ -312,133 +490,82 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
                      const float* v_descale, void* workspace, size_t workspace_bytes,
                      void* stream) {
     t_detail[0] = '\0';
-    // ---------------------------------------------------------------- validation
-    const bool varlen = cu_seqlens_q != nullptr || cu_seqlens_k != nullptr;
-    // with no key rows at all (fixed length seqlen_k == 0, or varlen total 0) K and V may be NULL
-    const bool no_keys = seqlen_k == 0;
-    if (!q || !o || !lse || (!no_keys && (!k || !v)))
-        return fail(FA_ERR_INVALID_ARG, "q, k, v, o and lse must be non-NULL device pointers");
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-        return fail(FA_ERR_INVALID_ARG, "q, k, v, o and lse must be 16-byte aligned");
-    if (batch < 0 || heads < 1 || seqlen_q < 0 || seqlen_k < 0)
-        return fail(FA_ERR_INVALID_ARG, "need batch >= 0, heads >= 1, seqlen_q/k >= 0");
-    if (heads_k < 1 || heads % heads_k != 0)
-        return fail(FA_ERR_INVALID_ARG, "heads_k (%d) must be >= 1 and divide heads (%d)", heads_k,
-                    heads);
-    if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
-    if (!(softmax_scale > 0.0f) || !std::isfinite(softmax_scale))
-        return fail(FA_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
     if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_E4M3)
         return fail(FA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
-    if (dtype == FA_DTYPE_BF16 && (q_descale || k_descale || v_descale))
-        return fail(FA_ERR_INVALID_ARG, "descale pointers are only meaningful for FA_DTYPE_E4M3");
-    if ((q_descale && (reinterpret_cast<uintptr_t>(q_descale) & 3u)) ||
-        (k_descale && (reinterpret_cast<uintptr_t>(k_descale) & 3u)) ||
-        (v_descale && (reinterpret_cast<uintptr_t>(v_descale) & 3u)))
-        return fail(FA_ERR_INVALID_ARG, "descale pointers must be 4-byte aligned");
-    if (varlen && (!cu_seqlens_q || !cu_seqlens_k))
-        return fail(FA_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k must both be given");
-    if (varlen && (max_seqlen_q < 0 || max_seqlen_k < 0))
-        return fail(FA_ERR_INVALID_ARG, "max_seqlen_q/k must be >= 0 for varlen");
-    if (head_dim != head_dim_v)
-        return fail(FA_ERR_UNSUPPORTED, "head_dim (%d) != head_dim_v (%d) is not built", head_dim,
-                    head_dim_v);
-    if (dtype == FA_DTYPE_BF16 && head_dim != 64 && head_dim != 128)
-        return fail(FA_ERR_UNSUPPORTED, "bf16 head_dim %d not built (64, 128)", head_dim);
-    if (dtype == FA_DTYPE_E4M3 && head_dim != 128)
-        return fail(FA_ERR_UNSUPPORTED, "e4m3 head_dim %d not built (128)", head_dim);
-    const long long rows_q = varlen ? seqlen_q : (long long)batch * seqlen_q;
-    const long long rows_k = varlen ? seqlen_k : (long long)batch * seqlen_k;
-    if (rows_q * heads * head_dim >= (1ll << 40) || rows_k * heads_k * head_dim >= (1ll << 40))
-        return fail(FA_ERR_INVALID_ARG, "tensor too large");
-    if (rows_q >= (1ll << 31) || rows_k >= (1ll << 31))
-        return fail(FA_ERR_INVALID_ARG, "row count must fit in int32");
-    const int mq = varlen ? max_seqlen_q : seqlen_q;
-    const int mk = varlen ? max_seqlen_k : seqlen_k;
-    if (batch == 0 || rows_q == 0 || mq == 0) return FA_OK;  // nothing to compute
+    FwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+    a.batch = batch; a.heads = heads; a.heads_k = heads_k;
+    a.seqlen_q = seqlen_q; a.seqlen_k = seqlen_k;
+    a.cu_q = cu_seqlens_q; a.cu_k = cu_seqlens_k;
+    a.max_q = max_seqlen_q; a.max_k = max_seqlen_k;
+    a.head_dim = head_dim; a.head_dim_v = head_dim_v;
+    a.scale = softmax_scale; a.causal = causal;
+    a.dtype = dtype; a.v_dtype = dtype;
+    a.qd = q_descale; a.kd = k_descale; a.vd = v_descale;
+    a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+    a.stream = stream;
+    return fwd_impl(a);
+}
 
-    int dev, sms;
-    uint32_t* err;
-    fa_status st = device_info(&dev, &sms, &err);
-    if (st != FA_OK) return st;
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int batch,
+                     int heads, int heads_k, int seqlen_q, int seqlen_k,
+                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int max_seqlen_q,
+                     int max_seqlen_k, int head_dim, float softmax_scale, int causal,
+                     fa_dtype v_dtype, const float* q_descale, const float* k_descale,
+                     const float* v_descale, int64_t descale_stride_b, int64_t descale_stride_h,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+    t_detail[0] = '\0';
+    FwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+    a.batch = batch; a.heads = heads; a.heads_k = heads_k;
+    a.seqlen_q = seqlen_q; a.seqlen_k = seqlen_k;
+    a.cu_q = cu_seqlens_q; a.cu_k = cu_seqlens_k;
+    a.max_q = max_seqlen_q; a.max_k = max_seqlen_k;
+    a.head_dim = head_dim; a.head_dim_v = head_dim;
+    a.scale = softmax_scale; a.causal = causal;
+    a.dtype = FA_DTYPE_E4M3; a.v_dtype = v_dtype;
+    a.qd = q_descale; a.kd = k_descale; a.vd = v_descale;
+    a.ds_b = descale_stride_b; a.ds_h = descale_stride_h;
+    a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+    a.stream = stream;
+    return fwd_impl(a);
+}
 
-    // ---------------------------------------------------------------- decomposition
-    int splits = 1;
-    if (!varlen && workspace) {
-        splits = choose_splits(batch, heads, seqlen_q, seqlen_k, causal, sms);
-        const size_t need = workspace_bytes_for(splits, batch, heads, seqlen_q, head_dim_v);
-        if (workspace_bytes < need)
-            return fail(FA_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed", workspace_bytes,
-                        need);
-        if (!aligned16(workspace)) return fail(FA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-    }
-    FwdParams p{};
-    p.o = o;
-    p.lse = lse;
-    p.cu_q = cu_seqlens_q;
-    p.cu_k = cu_seqlens_k;
-    p.q_descale = q_descale;
-    p.k_descale = k_descale;
-    p.v_descale = v_descale;
-    p.err = err;
-    p.batch = batch;
-    p.heads = heads;
-    p.kv_group = heads / heads_k;
-    p.seqlen_q = mq;
-    p.seqlen_k = mk;
-    p.total_q = varlen ? seqlen_q : 0;
-    p.n_mpairs = ceil_div(mq, 256);
-    p.n_splits = splits;
-    const int nblk = ceil_div(mk > 0 ? mk : 1, 128);
-    p.blocks_per_split = splits > 1 ? ceil_div(nblk, splits) : (1 << 29);
-    const long long n_items = (long long)p.n_mpairs * batch * heads * splits;
-    if (n_items >= (1ll << 31)) return fail(FA_ERR_INVALID_ARG, "too many work items");
-    p.n_items = (int)n_items;
-    p.scale_log2 = softmax_scale * 1.4426950408889634f;
-    p.causal = causal;
-    p.varlen = varlen ? 1 : 0;
-    p.split = splits > 1 ? 1 : 0;
-    if (p.split) {
-        const size_t rows = (size_t)splits * batch * heads * seqlen_q;
-        p.ws_o = static_cast<float*>(workspace);
-        p.ws_lse = p.ws_o + rows * head_dim_v;
-    }
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        p.wait_limit_ns = g_wait_limit_ns;
-        p.inject = g_inject;
-    }
-
-    // ---------------------------------------------------------------- tensor maps
-    const bool fp8 = dtype == FA_DTYPE_E4M3;
-    CUtensorMap tq, tk, tv;
-    // fixed length: (d, head, seq row, batch); varlen: (d, head, packed row, 1)
-    const int nbat = varlen ? 1 : batch;
-    if ((st = encode_map(&tq, q, fp8, head_dim, heads, seqlen_q, nbat)) != FA_OK) return st;
-    if (no_keys) {  // no key block is ever loaded; any valid map will do
-        tk = tq;
-        tv = tq;
-    } else {
-        if ((st = encode_map(&tk, k, fp8, head_dim, heads_k, seqlen_k, nbat)) != FA_OK) return st;
-        if ((st = encode_map(&tv, v, fp8, head_dim, heads_k, seqlen_k, nbat)) != FA_OK) return st;
-    }
-
-    // ---------------------------------------------------------------- launch
-    const int grid = (int)(n_items < sms ? n_items : sms);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (fp8)
-        e = launch_fwd_e4m3_d128(tq, tk, tv, p, grid, s);
-    else if (head_dim == 64)
-        e = launch_fwd_bf16_d64(tq, tk, tv, p, grid, s);
-    else
-        e = launch_fwd_bf16_d128(tq, tk, tv, p, grid, s);
-    if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
-    if (p.split) {
-        e = launch_combine(p.ws_o, p.ws_lse, o, lse, batch, heads, seqlen_q, head_dim_v, splits, s);
-        if (e != cudaSuccess) return fail(FA_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
-    }
-    return FA_OK;
+fa_status fa_fwd_kvcache(const void* q, void* k_cache, void* v_cache, const void* k_new,
+                         const void* v_new, void* o, float* lse, int batch, int heads, int heads_k,
+                         int seqlen_q, int cache_capacity, const int32_t* cache_seqlens,
+                         int seqlen_new, int head_dim, float softmax_scale, int causal,
+                         fa_dtype dtype, fa_dtype v_dtype, const float* q_descale,
+                         const float* k_descale, const float* v_descale,
+                         int64_t descale_stride_b, int64_t descale_stride_h, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    t_detail[0] = '\0';
+    if (!k_cache || !v_cache || !cache_seqlens)
+        return fail(FA_ERR_INVALID_ARG, "k_cache, v_cache and cache_seqlens must be non-NULL");
+    if (cache_capacity < 1 || seqlen_new < 0 || seqlen_new > cache_capacity)
+        return fail(FA_ERR_INVALID_ARG, "need cache_capacity >= 1 and 0 <= seqlen_new <= capacity");
+    if (seqlen_new > 0 && (!k_new || !v_new))
+        return fail(FA_ERR_INVALID_ARG, "k_new and v_new must be given when seqlen_new > 0");
+    if (seqlen_new > 0 && (!aligned16(k_new) || !aligned16(v_new)))
+        return fail(FA_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(cache_seqlens) & 3u) != 0)
+        return fail(FA_ERR_INVALID_ARG, "cache_seqlens must be 4-byte aligned");
+    if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_E4M3)
+        return fail(FA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    FwdArgs a{};
+    a.q = q; a.k = k_cache; a.v = v_cache; a.o = o; a.lse = lse;
+    a.batch = batch; a.heads = heads; a.heads_k = heads_k;
+    a.seqlen_q = seqlen_q; a.seqlen_k = cache_capacity;
+    a.head_dim = head_dim; a.head_dim_v = head_dim;
+    a.scale = softmax_scale; a.causal = causal;
+    a.dtype = dtype; a.v_dtype = v_dtype;
+    a.qd = q_descale; a.kd = k_descale; a.vd = v_descale;
+    a.ds_b = descale_stride_b; a.ds_h = descale_stride_h;
+    a.seqused_k = cache_seqlens; a.seqused_add = seqlen_new;
+    a.k_new = k_new; a.v_new = v_new; a.n_new = seqlen_new;
+    a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+    a.stream = stream;
+    return fwd_impl(a);
 }
 
 }  // extern "C"

@@ -116,6 +116,8 @@ struct Cfg {
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1 KiB
     static constexpr uint32_t kIdescQK = make_idesc(kBM, kBN, 0u + (FP8 ? 0u : 1u), false);
     static constexpr uint32_t kIdescPV = make_idesc(kBM, D, 0u + (FP8 ? 0u : 1u), true);
+    // FP8 with an E5M2 V: P (A operand) stays E4M3, B = V is E5M2 (kind::f8f6f4 codes 0 / 1)
+    static constexpr uint32_t kIdescPV5 = make_idesc2(kBM, D, 0u, 1u, true);
     static constexpr uint32_t kColO = 256;
     static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle atoms");
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KiB per-block shared memory");
@@ -132,6 +134,7 @@ struct Item {
     int n_lo, n_hi;      // key blocks [n_lo, n_hi) are visited, in reverse
     int n_hi_t[kTiles];  // tile t visits [n_lo, n_hi_t[t]); none if n_hi_t[t] <= n_lo
     bool active[kTiles]; // tile t has at least one row inside the sequence
+    bool bad_len;        // the per-sequence key length was out of range (clamped)
 };
 
 // Longest-processing-time order: item index -> pair index descending (under a
@@ -157,6 +160,12 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int w) {
         it.sq = p.seqlen_q;
         it.k_row0 = it.b * p.seqlen_k;
         it.sk = p.seqlen_k;
+    }
+    it.bad_len = false;
+    if (p.seqused_k) {  // a cache of capacity seqlen_k filled to this sequence's length
+        const int u = __ldg(p.seqused_k + it.b) + p.seqused_add;
+        it.bad_len = u < 0 || u > p.seqlen_k;
+        it.sk = min(max(u, 0), p.seqlen_k);
     }
     const int nblk = (it.sk + kBN - 1) / kBN;
     it.n_lo = it.split * p.blocks_per_split;
@@ -374,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // O_t += P_t V : A = P_t from TMEM, B = V (MN-major, 128B-swizzled):
             // leading offset = next 128-byte column atom, stride offset = next 8 keys.
+            const uint32_t idesc_pv = (FP8 && p.v_e5m2) ? C::kIdescPV5 : C::kIdescPV;
             auto issue_pv = [&](auto tc, uint32_t vslot, uint32_t acc) {
                 constexpr int t = decltype(tc)::value;
                 const uint32_t b0 = v_lo + vslot * kTile16;
@@ -382,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t off = (uint32_t)(kk * C::kUmmaK * 128) >> 4;
                     const uint32_t a_tmem = tmem_base + 128u * t + 8u * kk;
                     if constexpr (FP8)
-                        umma_f8_ts(tmem_base + C::kColO + 128u * t, a_tmem, desc(b0 + off), C::kIdescPV,
+                        umma_f8_ts(tmem_base + C::kColO + 128u * t, a_tmem, desc(b0 + off), idesc_pv,
                                    kk > 0 ? 1u : acc);
                     else
                         umma_f16_ts(tmem_base + C::kColO + 128u * t, a_tmem, desc(b0 + off), C::kIdescPV,
@@ -492,14 +502,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t t_lane = tmem_base + ((uint32_t)(wq * 32) << 16);
         const uint32_t t_s = t_lane + 128u * t;     // S_t (fp32) and, over it, P_t
         const uint32_t t_o = t_lane + C::kColO + 128u * t;
-        float scale_log2 = p.scale_log2;
-        float o_scale = 1.0f;
-        if constexpr (FP8) {
-            const float qd = p.q_descale ? __ldg(p.q_descale) : 1.0f;
-            const float kd = p.k_descale ? __ldg(p.k_descale) : 1.0f;
-            scale_log2 *= qd * kd;
-            o_scale = p.v_descale ? __ldg(p.v_descale) : 1.0f;
-        }
         uint32_t s_cnt = 0, o_cnt = 0;
         uint32_t kv_base = 0;  // ring position of the current item's first K/V load
         const bool releaser = wq == 0 && lane == 0;  // this warpgroup's slot-release thread
@@ -508,6 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int w = item_of_round(round, nctas);
             if (w >= p.n_items) break;
             const Item it = decode_item(p, w);
+            if (it.bad_len && r_in_tile == 0 && t == 0) atomicOr(p.err, kErrBadLength);
             const uint32_t item_base = kv_base;
             if (it.n_hi > it.n_lo) kv_base += 2u * (uint32_t)(it.n_hi - it.n_lo);
             // ring slots of this item's K(j) and V(j)
@@ -518,6 +521,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t_m0 = t ? it.m0[1] : it.m0[0];
             const int t_hi = t ? it.n_hi_t[1] : it.n_hi_t[0];
             if (!t_active) continue;
+            // FP8: q_descale * k_descale folded into the scale of this work tile, which
+            // belongs to one (batch, head); v_descale scales its output
+            float scale_log2 = p.scale_log2;
+            float o_scale = 1.0f;
+            if constexpr (FP8) {
+                const long long ds = it.b * p.descale_sb + (long long)(it.h / p.kv_group) * p.descale_sh;
+                const float qd = p.q_descale ? __ldg(p.q_descale + ds) : 1.0f;
+                const float kd = p.k_descale ? __ldg(p.k_descale + ds) : 1.0f;
+                scale_log2 *= qd * kd;
+                o_scale = p.v_descale ? __ldg(p.v_descale + ds) : 1.0f;
+            }
             const int row = t_m0 + r_in_tile;  // row within the sequence
             const bool row_ok = row < it.sq;
             // output addresses

@@ -15,9 +15,13 @@ struct FwdParams {
     float* lse;                 // fp32 LSE (or unused in split mode)
     const int32_t* cu_q;        // varlen offsets (device) or nullptr
     const int32_t* cu_k;
-    const float* q_descale;     // FP8 only, device scalars or nullptr (= 1)
-    const float* k_descale;
-    const float* v_descale;
+    const float* q_descale;     // FP8 only, device arrays or nullptr (= 1); the descale of
+    const float* k_descale;     //   (batch b, query head h) is at b * descale_sb +
+    const float* v_descale;     //   (h / kv_group) * descale_sh (0, 0: one value per tensor)
+    long long descale_sb, descale_sh;
+    const int32_t* seqused_k;   // fixed length: keys of sequence b = seqused_k[b] + seqused_add
+    int seqused_add;            //   (nullptr: seqlen_k); lengths outside [0, seqlen_k] are clamped
+                                //   and flagged in the device error word
     float* ws_o;                // split mode: normalised partial O [splits, B, H, Sq, Dv] fp32
     float* ws_lse;              // split mode: partial LSE [splits, B, H, Sq] fp32
     uint32_t* err;              // device error word
@@ -31,11 +35,12 @@ struct FwdParams {
     int n_items;                // n_mpairs * batch * heads * n_splits
     float scale_log2;           // softmax_scale * log2(e)
     int causal, varlen, split;
+    int v_e5m2;                 // FP8: V stored as E5M2 (Q, K and P stay E4M3)
     uint64_t wait_limit_ns;     // bound of every device-side wait
     uint32_t inject;            // debug fault injection (see fa_debug_set)
 };
 
-enum : uint32_t { kErrTimeout = 1u };
+enum : uint32_t { kErrTimeout = 1u, kErrBadLength = 2u };
 
 // Kernel instances (one translation unit each).
 cudaError_t launch_fwd_bf16_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
@@ -44,6 +49,9 @@ cudaError_t launch_fwd_bf16_d128(const CUtensorMap& q, const CUtensorMap& k, con
                                  const FwdParams& p, int grid, cudaStream_t s);
 cudaError_t launch_fwd_e4m3_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                  const FwdParams& p, int grid, cudaStream_t s);
+cudaError_t launch_append_kv(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                             const int32_t* cache_seqlens, int batch, int capacity, int n_new,
+                             long long row_bytes, uint32_t* err, cudaStream_t s);
 cudaError_t launch_combine(const float* ws_o, const float* ws_lse, void* o, float* lse,
                            int batch, int heads, int seqlen_q, int dv, int n_splits,
                            cudaStream_t s);

@@ -228,10 +228,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 //   15 A major (0 = K-major), 16 B major (1 = MN-major),
 //   17-22 N >> 3, 24-28 M >> 4.
 // A/B format codes: kind::f16 -> 0 f16, 1 bf16; kind::f8f6f4 -> 0 e4m3, 1 e5m2.
+__host__ __device__ constexpr uint32_t make_idesc2(int m, int n, uint32_t a_format,
+                                                   uint32_t b_format, bool b_mn_major) {
+    return (1u << 4) | (a_format << 7) | (b_format << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+// A and B of one format (kind::f16 requires that; kind::f8f6f4 allows A and B to differ)
 __host__ __device__ constexpr uint32_t make_idesc(int m, int n, uint32_t ab_format,
                                                   bool b_mn_major) {
-    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+    return make_idesc2(m, n, ab_format, ab_format, b_mn_major);
 }
 
 // ---------------------------------------------------------------- math

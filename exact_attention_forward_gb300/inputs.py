@@ -16,6 +16,9 @@ Workloads (shapes and value distributions of the attention configurations):
   bf16_gqa_causal_8k  B=2  H=32 (8 K/V heads) S=8192 D=128 2*N(0,1) causal seed 1007
   fp8_headscale_4k    B=4  H=16 S=4096 D=128 Q/K e4m3, V e5m2, one descale per
                       (batch, head) = amax/max-finite       non-causal  seed 1008
+  bf16_kvcache_decode B=16 H=32 (8 K/V heads) D=128, a K/V cache of capacity 8192
+                      filled to U{4096..8191} rows per sequence; one new token
+                      (q, k_new, v_new of 1 row) appended, then attended   seed 1009
 """
 from __future__ import annotations
 
@@ -48,6 +51,8 @@ class Workload:
     n_seqs: int = 0
     empty_k_at: tuple = ()       # packed positions of sequences with seqlen_k = 0
     heads_k: int = 0             # K/V heads (grouped-query attention); 0 = heads
+    cache_new: int = 0           # > 0: K/V cache workload; seqlen_k is the cache capacity,
+                                 #   seqlen_q = cache_new new rows are appended, then attended
 
     @property
     def softmax_scale(self) -> float:
@@ -76,6 +81,9 @@ WORKLOADS = {
     # FP8 with one descale per (batch, head) and an E5M2 V
     "fp8_headscale_4k": Workload("fp8_headscale_4k", 4, 16, 4096, 4096, 128, False,
                                  dtype="e4m3", v_dtype="e5m2", descale="head", seed=1008),
+    # decoding with a key/value cache: append one token, attend over the filled cache
+    "bf16_kvcache_decode": Workload("bf16_kvcache_decode", 16, 32, 1, 8192, 128, True,
+                                    seed=1009, heads_k=8, cache_new=1),
 }
 
 
@@ -102,7 +110,8 @@ def quantize_fp8_per_head(x: torch.Tensor, fmt: str, heads_k: int):
     dt, mx = _FP8[fmt]
     B, S, H, D = x.shape
     g = x.reshape(B, S, heads_k, H // heads_k, D)
-    amax = g.abs().amax(dim=(1, 3, 4))                        # [B, heads_k]
+    amax = (g.abs().amax(dim=(1, 3, 4)) if g.numel() else     # [B, heads_k]
+            torch.zeros((B, heads_k), dtype=x.dtype))
     descale = torch.where(amax > 0, amax / mx, torch.ones_like(amax)).to(torch.float32)
     y = (g / descale.view(B, 1, heads_k, 1, 1)).clamp_(-mx, mx).reshape(B, S, H, D)
     return y.to(dt), descale
@@ -131,8 +140,10 @@ def varlen_lengths(w: Workload, gen: torch.Generator):
 def make_inputs(w: Workload, *, seed: Optional[int] = None, shapes_only_q: Optional[int] = None):
     """Draw (on the CPU) the inputs of a workload.
 
-    Returns a dict with q, k, v (bf16 or float8, CPU), descale (q, k, v: python
-    floats, or fp32 [B, Hk] tensors for per-head descales),
+    Returns a dict with q, k, v (bf16 or float8, CPU; for cache workloads k and v
+    are the caches [B, capacity, Hk, D]), descale (q, k, v: python floats, or fp32
+    [B, Hk] tensors for per-head descales), k_new / v_new / cache_seqlens (cache
+    workloads; drawn after Q, K, V),
     cu_seqlens_q/k (int32 CPU tensors or None), max_seqlen_q/k, seqlens.
     Draw order: Q, K, V (fp32 N(0,1), times amp), then varlen lengths.
     For varlen, the lengths are drawn first from their own generator stream
@@ -158,6 +169,20 @@ def make_inputs(w: Workload, *, seed: Optional[int] = None, shapes_only_q: Optio
     q = torch.randn(q_shape, generator=gen, dtype=torch.float32)
     k = torch.randn(k_shape, generator=gen, dtype=torch.float32)
     v = torch.randn(k_shape, generator=gen, dtype=torch.float32)
+    cache = {}
+    if w.cache_new:
+        # new rows, then the filled length of each sequence's cache (rows past it are
+        # random too: they must be ignored)
+        nshape = (w.batch, w.cache_new, w.kv_heads, w.head_dim)
+        cache["k_new"] = torch.randn(nshape, generator=gen, dtype=torch.float32) * w.amp
+        cache["v_new"] = torch.randn(nshape, generator=gen, dtype=torch.float32) * w.amp
+        lo = w.seqlen_k // 2
+        cache["cache_seqlens"] = torch.randint(lo, w.seqlen_k - w.cache_new + 1, (w.batch,),
+                                               generator=gen, dtype=torch.int32)
+        if w.dtype != "bf16":
+            raise ValueError("cache workloads are drawn in bf16")
+        cache["k_new"] = cache["k_new"].to(torch.bfloat16)
+        cache["v_new"] = cache["v_new"].to(torch.bfloat16)
     if w.amp != 1.0:
         q.mul_(w.amp)
         k.mul_(w.amp)
@@ -180,7 +205,7 @@ def make_inputs(w: Workload, *, seed: Optional[int] = None, shapes_only_q: Optio
         q, k, v = q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
         descale = (1.0, 1.0, 1.0)
     return dict(q=q, k=k, v=v, descale=descale, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
-                max_seqlen_q=max_q, max_seqlen_k=max_k, seqlens=seqlens)
+                max_seqlen_q=max_q, max_seqlen_k=max_k, seqlens=seqlens, **cache)
 
 
 def make_random(batch, heads, seqlen_q, seqlen_k, head_dim, *, seed, amp=1.0,

@@ -55,12 +55,14 @@ typedef enum {
     FA_ERR_UNSUPPORTED = 2,     /* valid but not built: head_dim not in {64,128}, ... */
     FA_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed (launch, tensor map) */
     FA_ERR_WORKSPACE = 4,       /* workspace given but smaller than fa_fwd_workspace_size() */
-    FA_ERR_DEVICE_TIMEOUT = 5   /* a bounded device-side wait gave up (see fa_device_error) */
+    FA_ERR_DEVICE_TIMEOUT = 5,  /* a bounded device-side wait gave up (see fa_device_error) */
+    FA_ERR_DEVICE_ARG = 6       /* a device-resident length was out of range (fa_device_error) */
 } fa_status;
 
 typedef enum {
     FA_DTYPE_BF16 = 0,          /* Q, K, V bfloat16 */
-    FA_DTYPE_E4M3 = 1           /* Q, K, V float8 e4m3 (OCP "fn"), per-tensor descales */
+    FA_DTYPE_E4M3 = 1,          /* float8 e4m3 (OCP "fn": no infinities, max 448) */
+    FA_DTYPE_E5M2 = 2           /* float8 e5m2 (OCP, max 57344): accepted for V only */
 } fa_dtype;
 
 /*
@@ -126,6 +128,75 @@ FA_API fa_status fa_fwd_gqa(const void* q, const void* k, const void* v,
                             void* stream);
 
 /*
+ * fa_fwd_fp8 -- FP8 attention with per-(batch, head) descales and an optional
+ * E5M2 V.  The page "FlashAttention core algorithm: forward pass" (consumer
+ * mainloop excerpt, FP8 branch) multiplies the softmax scale of a work tile by
+ * q_descale * k_descale; a work tile belongs to one (batch, head), so here each
+ * (batch b, key/value head g) has its own descales:
+ *     q/k/v_descale[b * descale_stride_b + g * descale_stride_h]
+ * (device fp32; query head h uses g = h / (heads / heads_k); strides in
+ * elements, >= 0; strides 0, 0 = one value per tensor as in fa_fwd; a NULL
+ * descale means 1).  Scores use softmax_scale * q_descale * k_descale and the
+ * output row is multiplied by v_descale.  The arrays must hold every index the
+ * strides reach for b < batch, g < heads_k (not checked: device memory).
+ * q, k: E4M3.  v_dtype: FA_DTYPE_E4M3 or FA_DTYPE_E5M2 (P is rounded to E4M3
+ * either way).  head_dim = head_dim_v = 128.  All else as fa_fwd_gqa, whose
+ * layouts, workspace rules and errors apply.
+ */
+FA_API fa_status fa_fwd_fp8(const void* q, const void* k, const void* v,
+                            void* o, float* lse,
+                            int batch, int heads, int heads_k, int seqlen_q, int seqlen_k,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int max_seqlen_q, int max_seqlen_k,
+                            int head_dim, float softmax_scale, int causal,
+                            fa_dtype v_dtype,
+                            const float* q_descale, const float* k_descale,
+                            const float* v_descale,
+                            int64_t descale_stride_b, int64_t descale_stride_h,
+                            void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * fa_fwd_kvcache -- append new key/value rows to a key/value cache, then attend
+ * over the cache.  The AppendKV branch of the producer loop on the page
+ * "FlashAttention core algorithm: forward pass" (scheduler-loop excerpt) loads
+ * the new K/V before the attention of the same work tile; here the rows are
+ * first written into the cache by a copy kernel, then the forward kernel runs,
+ * both on `stream`.
+ *   q        [batch, seqlen_q, heads, head_dim]
+ *   k_cache, v_cache [batch, cache_capacity, heads_k, head_dim]   (written)
+ *   k_new, v_new     [batch, seqlen_new, heads_k, head_dim] or NULL (seqlen_new 0)
+ *   cache_seqlens    device int32 [batch]: rows already filled in each sequence
+ *                    (read only: the caller advances it by seqlen_new afterwards)
+ *   o [batch, seqlen_q, heads, head_dim] bf16, lse [batch, heads, seqlen_q] fp32
+ * Sequence b: rows cache_seqlens[b] .. + seqlen_new - 1 of the caches receive
+ * k_new[b] / v_new[b]; then query row i attends over the first
+ * L_b = cache_seqlens[b] + seqlen_new cache rows, with causal = 1 bottom-right
+ * aligned (key j visible iff j <= i + L_b - seqlen_q).  L_b = 0 gives O = 0 and
+ * LSE = -inf.  dtype / v_dtype / descales as fa_fwd (bf16) or fa_fwd_fp8 (FP8;
+ * new rows must already be quantised with the cache's descales: bytes are copied).
+ * cache_seqlens lives on the device, so it is checked there: a sequence with
+ * cache_seqlens[b] < 0 or cache_seqlens[b] + seqlen_new > cache_capacity gets no
+ * rows appended, its attention uses the length clamped to [0, capacity], and
+ * fa_device_error() afterwards returns FA_ERR_DEVICE_ARG.  workspace: as fa_fwd
+ * (key splits for short-query / long-cache shapes, sized by
+ * fa_fwd_workspace_size(batch, heads, seqlen_q, cache_capacity, head_dim, causal)).
+ */
+FA_API fa_status fa_fwd_kvcache(const void* q, void* k_cache, void* v_cache,
+                                const void* k_new, const void* v_new,
+                                void* o, float* lse,
+                                int batch, int heads, int heads_k, int seqlen_q,
+                                int cache_capacity, const int32_t* cache_seqlens,
+                                int seqlen_new,
+                                int head_dim, float softmax_scale, int causal,
+                                fa_dtype dtype, fa_dtype v_dtype,
+                                const float* q_descale, const float* k_descale,
+                                const float* v_descale,
+                                int64_t descale_stride_b, int64_t descale_stride_h,
+                                void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/*
  * Bytes of workspace that fa_fwd would use to split the key range of a
  * fixed-length problem of this shape on the current device (0 = it would not
  * split).  Splitting follows the log-sum-exp merge identity: each split
@@ -176,9 +247,11 @@ FA_API const char* fa_last_error_detail(void);
  * device-resident error word, the kernel's CTAs abandon their work and exit
  * cleanly (TMEM released), and the context stays usable.
  * fa_device_error synchronises the current device, copies the word to
- * *flags (bit 0: a wait timed out; bits 8..15: the site of the first
- * timeout) and, if clear != 0, resets it.  Returns FA_ERR_DEVICE_TIMEOUT if
- * a timeout bit was set, FA_OK otherwise (FA_ERR_CUDA on a CUDA failure).
+ * *flags (bit 0: a wait timed out; bit 1: a device-resident cache length was
+ * out of range; bits 8..15: the site of the first timeout) and, if clear != 0,
+ * resets it.  Returns FA_ERR_DEVICE_TIMEOUT if a timeout bit was set, else
+ * FA_ERR_DEVICE_ARG if the length bit was set, FA_OK otherwise (FA_ERR_CUDA on
+ * a CUDA failure).
  */
 FA_API fa_status fa_device_error(uint32_t* flags, int clear);
 

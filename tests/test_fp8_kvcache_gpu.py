@@ -1,0 +1,198 @@
+"""GPU parity of the FP8 variant with per-(batch, head) descales and an E5M2 V,
+and of the key/value-cache path (append new rows, then attend over the first
+cache_seqlens + seqlen_new rows of each sequence), against the fp64 oracle.
+
+The FP8 descales here differ per batch and per K/V head, so a descale read for
+the wrong (batch, head) fails the comparison; V is stored as E5M2 while P is
+rounded to E4M3 inside the kernel.  The cache cases compare the appended caches
+byte for byte with the oracle's append and the attention element by element.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import exact_attention_forward_gb300 as fa
+from exact_attention_forward_gb300 import inputs
+from parity_util import compare, gather_rows, run_gpu, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    fa.debug_set(0, 0)
+    fa.device_error(clear=True)
+
+
+# ---------------------------------------------------------------------------- FP8
+def _fp8_head_inputs(B, H, Hk, Sq, Sk, v_dtype, seed):
+    """N(0,1) rows scaled per (batch, head) by factors in [0.75, 1] (so that every
+    (batch, K/V head) gets a different descale while the values keep the spread of
+    the FP8 workload, for which the 6e-2 bound is stated), quantised per (batch,
+    K/V head)."""
+    g = torch.Generator().manual_seed(seed)
+    f = lambda heads: 0.75 + 0.25 * torch.rand((B, 1, heads, 1), generator=g)
+    q = torch.randn((B, Sq, H, 128), generator=g) * f(H)
+    k = torch.randn((B, Sk, Hk, 128), generator=g) * f(Hk)
+    v = torch.randn((B, Sk, Hk, 128), generator=g) * f(Hk)
+    q8, dq = inputs.quantize_fp8_per_head(q, "e4m3", Hk)
+    k8, dk = inputs.quantize_fp8_per_head(k, "e4m3", Hk)
+    v8, dv = inputs.quantize_fp8_per_head(v, v_dtype, Hk)
+    return dict(q=q8, k=k8, v=v8, descale=(dq, dk, dv))
+
+
+@pytest.mark.parametrize("B,H,Hk,Sq,Sk,causal,v_dtype", [
+    (2, 4, 4, 300, 400, False, "e5m2"),
+    (2, 4, 2, 300, 400, True, "e5m2"),
+    (3, 6, 3, 129, 257, True, "e4m3"),     # per-head descales with an E4M3 V
+    (1, 8, 1, 128, 3000, False, "e5m2"),   # multi-query; splits the key range
+])
+def test_fp8_head_descales_full(B, H, Hk, Sq, Sk, causal, v_dtype):
+    x = _fp8_head_inputs(B, H, Hk, Sq, Sk, v_dtype, seed=200 + H + Hk + Sq)
+    assert x["descale"][0].shape == (B, Hk)
+    o, lse = run_gpu(x, causal=causal, softmax_scale=128 ** -0.5)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=128 ** -0.5,
+                                      causal=causal, descale=x["descale"])
+    compare(o, lse, o_ref, lse_ref, dtype="e4m3",
+            what=f"fp8 per-head {(B, H, Hk, Sq, Sk, causal, v_dtype)}")
+    if B * Hk == 1:
+        return
+    # the descales really differ per (batch, head): a kernel that read one value for
+    # the whole tensor would be far off
+    o1, lse1 = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=128 ** -0.5, causal=causal,
+                                descale=tuple(float(d[0, 0]) for d in x["descale"]))
+    assert np.abs(lse1 - lse_ref).max() > 0.1
+
+
+def test_fp8_headscale_workload_sampled():
+    w = inputs.WORKLOADS["fp8_headscale_4k"]
+    x = inputs.make_inputs(w)
+    assert x["v"].dtype == torch.float8_e5m2
+    o, lse = run_gpu(x, causal=w.causal, softmax_scale=w.softmax_scale)
+    rows = sample_rows(w.batch, w.heads, w.seqlen_q, 256, seed=8)
+    o_ref, lse_ref = oracle.attention_rows(x["q"], x["k"], x["v"], rows,
+                                           softmax_scale=w.softmax_scale, causal=w.causal,
+                                           descale=x["descale"])
+    og, lg = gather_rows(o, lse, rows)
+    compare(og, lg, o_ref, lse_ref, dtype="e4m3", what=w.name)
+
+
+def test_fp8_head_descales_varlen():
+    # one descale per (sequence, K/V head), each sequence quantised with its own
+    seq_q, seq_k, H, Hk = [40, 300, 0, 129], [40, 300, 5, 200], 4, 2
+    g = torch.Generator().manual_seed(210)
+    cq = torch.tensor([0] + list(np.cumsum(seq_q)), dtype=torch.int32)
+    ck = torch.tensor([0] + list(np.cumsum(seq_k)), dtype=torch.int32)
+    parts = {"q": [], "k": [], "v": []}
+    ds = {"q": [], "k": [], "v": []}
+    for b in range(len(seq_q)):
+        for n, s, heads, fmt in (("q", seq_q[b], H, "e4m3"), ("k", seq_k[b], Hk, "e4m3"),
+                                 ("v", seq_k[b], Hk, "e5m2")):
+            x = torch.randn((1, s, heads, 128), generator=g) * (0.7 + 0.1 * b)
+            x8, d = inputs.quantize_fp8_per_head(x, fmt, Hk)
+            parts[n].append(x8[0])
+            ds[n].append(d[0])
+    x = dict(q=torch.cat(parts["q"]), k=torch.cat(parts["k"]), v=torch.cat(parts["v"]),
+             descale=tuple(torch.stack(ds[n]) for n in "qkv"), cu_seqlens_q=cq, cu_seqlens_k=ck,
+             max_seqlen_q=max(seq_q), max_seqlen_k=max(seq_k))
+    o, lse = run_gpu(x, causal=True, softmax_scale=128 ** -0.5)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=128 ** -0.5,
+                                      causal=True, cu_seqlens_q=cq, cu_seqlens_k=ck,
+                                      descale=x["descale"])
+    compare(o, lse, o_ref, lse_ref, dtype="e4m3", what="fp8 per-head varlen")
+
+
+# ---------------------------------------------------------------------------- cache
+def _cache_case(B, H, Hk, Sq, cap, lens, n_new, *, seed, dtype="bf16", v_dtype=""):
+    """Caches filled with random rows everywhere (rows past each length must be ignored)."""
+    xc = inputs.make_random(B, H, Sq, cap, 128, seed=seed, dtype=dtype, heads_k=Hk,
+                            v_dtype=v_dtype, descale="head" if dtype == "e4m3" else "tensor")
+    new = None
+    if n_new:
+        xn = inputs.make_random(B, Hk, n_new, n_new, 128, seed=seed + 1, dtype=dtype, heads_k=Hk,
+                                v_dtype=v_dtype, descale="head" if dtype == "e4m3" else "tensor")
+        new = (xn["k"], xn["v"])  # (FP8: quantised with their own descales; only bytes matter)
+    return xc, new, torch.tensor(lens, dtype=torch.int32)
+
+
+def _run_cache(xc, new, lens, causal):
+    dev = "cuda"
+    kc, vc = xc["k"].to(dev).contiguous(), xc["v"].to(dev).contiguous()
+    kn = vn = None
+    if new is not None:
+        kn, vn = new[0].to(dev), new[1].to(dev)
+    fp8 = xc["q"].dtype == torch.float8_e4m3fn
+    o, lse = fa.fwd_kvcache(xc["q"].to(dev), kc, vc, lens.to(dev), kn, vn, causal=causal,
+                            descale=xc["descale"] if fp8 else None)
+    torch.cuda.synchronize()
+    return o, lse, kc, vc
+
+
+@pytest.mark.parametrize("B,H,Hk,Sq,cap,lens,n_new,causal", [
+    (3, 4, 2, 37, 1000, [0, 517, 900], 37, True),      # chunked prefill into a cache
+    (2, 4, 4, 200, 700, [300, 64], 0, False),           # attention only, no new rows
+    (4, 8, 2, 1, 8192, [8191, 4000, 0, 1], 1, True),    # decode: one new token, key splits
+    (2, 2, 1, 130, 520, [390, 0], 130, True),           # new rows fill the cache exactly
+])
+def test_kvcache_append_and_attend(B, H, Hk, Sq, cap, lens, n_new, causal):
+    xc, new, lens_t = _cache_case(B, H, Hk, Sq, cap, lens, n_new, seed=300 + Sq + n_new)
+    o, lse, kc, vc = _run_cache(xc, new, lens_t, causal)
+    st, flags = fa.device_error(clear=True)
+    assert st == fa.FA_OK, f"device error word {flags:#x}"
+    if new is not None:
+        k_ref = oracle.append_kv(xc["k"], new[0], lens)
+        v_ref = oracle.append_kv(xc["v"], new[1], lens)
+        assert torch.equal(kc.cpu().view(torch.int16), k_ref.view(torch.int16))
+        assert torch.equal(vc.cpu().view(torch.int16), v_ref.view(torch.int16))
+    else:
+        k_ref, v_ref = xc["k"], xc["v"]
+    used = [l + n_new for l in lens]
+    o_ref, lse_ref = oracle.attention(xc["q"], k_ref, v_ref, softmax_scale=128 ** -0.5,
+                                      causal=causal, seqused_k=used)
+    compare(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+            o_ref, lse_ref, what=f"kvcache {(B, H, Hk, Sq, cap, lens, n_new, causal)}")
+
+
+def test_kvcache_fp8_head_descales_e5m2_v():
+    B, H, Hk, Sq, cap, lens, n_new = 2, 8, 2, 64, 3000, [1000, 2500], 64
+    xc, new, lens_t = _cache_case(B, H, Hk, Sq, cap, lens, n_new, seed=333, dtype="e4m3",
+                                  v_dtype="e5m2")
+    assert xc["v"].dtype == torch.float8_e5m2
+    o, lse, kc, vc = _run_cache(xc, new, lens_t, True)
+    assert fa.device_error(clear=True)[0] == fa.FA_OK
+    k_ref = oracle.append_kv(xc["k"], new[0], lens)
+    v_ref = oracle.append_kv(xc["v"], new[1], lens)
+    assert torch.equal(kc.cpu().view(torch.uint8), k_ref.view(torch.uint8))
+    assert torch.equal(vc.cpu().view(torch.uint8), v_ref.view(torch.uint8))
+    o_ref, lse_ref = oracle.attention(xc["q"], k_ref, v_ref, softmax_scale=128 ** -0.5,
+                                      causal=True, seqused_k=[l + n_new for l in lens],
+                                      descale=xc["descale"])
+    compare(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+            o_ref, lse_ref, dtype="e4m3", what="kvcache fp8")
+
+
+def test_kvcache_out_of_range_length_is_reported_and_clamped():
+    B, H, Hk, Sq, cap, n_new = 2, 2, 2, 16, 300, 16
+    lens = [290, 100]  # 290 + 16 > 300: sequence 0 gets no rows, its length is clamped to 300
+    xc, new, lens_t = _cache_case(B, H, Hk, Sq, cap, lens, n_new, seed=340)
+    fa.device_error(clear=True)
+    o, lse, kc, vc = _run_cache(xc, new, lens_t, False)
+    st, flags = fa.device_error(clear=True)
+    assert st == fa.FA_ERR_DEVICE_ARG and flags & 2
+    # sequence 0: cache untouched, attention over all 300 rows; sequence 1: normal
+    assert torch.equal(kc[0].cpu().view(torch.int16), xc["k"][0].view(torch.int16))
+    k_ref = xc["k"].clone()
+    v_ref = xc["v"].clone()
+    k_ref[1, 100:116] = new[0][1]
+    v_ref[1, 100:116] = new[1][1]
+    assert torch.equal(kc.cpu().view(torch.int16), k_ref.view(torch.int16))
+    o_ref, lse_ref = oracle.attention(xc["q"], k_ref, v_ref, softmax_scale=128 ** -0.5,
+                                      seqused_k=[300, 116])
+    compare(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+            o_ref, lse_ref, what="kvcache clamped length")
+    # the context is still usable
+    o2, lse2, _, _ = _run_cache(*_cache_case(1, 2, 2, 8, 64, [10], 8, seed=341), False)
+    assert fa.device_error(clear=True)[0] == fa.FA_OK

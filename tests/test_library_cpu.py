@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(7):
         assert lib.fa_status_string(code)
     assert b"unknown" in lib.fa_status_string(99)
 
@@ -91,3 +91,66 @@ def test_gqa_validation(lib):
     assert gqa(8, 0) == fa.FA_ERR_INVALID_ARG
     assert gqa(8, 16) == fa.FA_ERR_INVALID_ARG
     assert b"heads_k" in lib.fa_last_error_detail()
+
+
+def fp8(lib, **kw):
+    a = dict(batch=1, heads=4, heads_k=2, sq=128, sk=128, d=128, vdt=fa.FA_DTYPE_E5M2, qd=P, kd=P,
+             vd=P, sb=2, sh=1)
+    a.update(kw)
+    return lib.fa_fwd_fp8(P, P, P, P, P, a["batch"], a["heads"], a["heads_k"], a["sq"], a["sk"],
+                          None, None, 0, 0, a["d"], 0.1, 0, a["vdt"], a["qd"], a["kd"], a["vd"],
+                          a["sb"], a["sh"], None, 0, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(vdt=fa.FA_DTYPE_BF16), fa.FA_ERR_INVALID_ARG),    # V type must be an FP8 type
+    (dict(vdt=9), fa.FA_ERR_INVALID_ARG),
+    (dict(sb=-1), fa.FA_ERR_INVALID_ARG),                   # negative descale stride
+    (dict(qd=ctypes.c_void_p(0x10002)), fa.FA_ERR_INVALID_ARG),  # misaligned descale
+    (dict(heads_k=3), fa.FA_ERR_INVALID_ARG),
+    (dict(d=64), fa.FA_ERR_UNSUPPORTED),
+])
+def test_fp8_validation(lib, kw, code):
+    assert fp8(lib, **kw) == code
+    assert lib.fa_last_error_detail()
+
+
+def test_fp8_empty_problem_is_ok_without_a_device(lib):
+    assert fp8(lib, batch=0) == fa.FA_OK
+
+
+def test_e5m2_only_accepted_for_v(lib):
+    # fa_fwd_gqa takes one type for q, k and v: E5M2 is not one of them
+    assert lib.fa_fwd_gqa(P, P, P, P, P, 1, 2, 2, 128, 128, None, None, 0, 0, 128, 128, 0.1, 0,
+                          fa.FA_DTYPE_E5M2, None, None, None, None, 0, None) == fa.FA_ERR_INVALID_ARG
+
+
+def kvc(lib, **kw):
+    a = dict(kc=P, vc=P, kn=P, vn=P, batch=2, heads=4, heads_k=2, sq=1, cap=4096, lens=P, n_new=1,
+             d=128, dt=fa.FA_DTYPE_BF16, vdt=fa.FA_DTYPE_BF16, qd=None)
+    a.update(kw)
+    return lib.fa_fwd_kvcache(P, a["kc"], a["vc"], a["kn"], a["vn"], P, P, a["batch"], a["heads"],
+                              a["heads_k"], a["sq"], a["cap"], a["lens"], a["n_new"], a["d"], 0.1,
+                              1, a["dt"], a["vdt"], a["qd"], None, None, 0, 0, None, 0, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(kc=None), fa.FA_ERR_INVALID_ARG),
+    (dict(lens=None), fa.FA_ERR_INVALID_ARG),
+    (dict(lens=ctypes.c_void_p(0x10002)), fa.FA_ERR_INVALID_ARG),
+    (dict(kn=None), fa.FA_ERR_INVALID_ARG),            # new rows announced but not given
+    (dict(vn=ctypes.c_void_p(0x10008)), fa.FA_ERR_INVALID_ARG),
+    (dict(n_new=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(n_new=5000), fa.FA_ERR_INVALID_ARG),         # more new rows than the capacity
+    (dict(cap=0), fa.FA_ERR_INVALID_ARG),
+    (dict(vdt=fa.FA_DTYPE_E5M2), fa.FA_ERR_INVALID_ARG),  # bf16 q/k with an FP8 V
+    (dict(qd=P), fa.FA_ERR_INVALID_ARG),               # descale with bf16
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+])
+def test_kvcache_validation(lib, kw, code):
+    assert kvc(lib, **kw) == code
+    assert lib.fa_last_error_detail()
+
+
+def test_kvcache_empty_batch_is_ok_without_a_device(lib):
+    assert kvc(lib, batch=0) == fa.FA_OK
