@@ -339,10 +339,12 @@ def run_gpu(args, w):
     lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
     ws = None
     if not w.varlen:
-        need = fa.workspace_size(w.batch, w.heads, w.seqlen_q, w.seqlen_k, w.head_dim, w.causal)
+        need = fa.workspace_size(w.batch, w.heads, w.seqlen_q, w.seqlen_k, w.head_dim, w.causal,
+                                 heads_k=w.kv_heads)
         if need:
             ws = torch.empty(need, dtype=torch.uint8, device=dev)
-    splits = fa.num_splits(w.batch, w.heads, w.seqlen_q, w.seqlen_k, w.causal) if ws is not None else 1
+    splits = (fa.num_splits(w.batch, w.heads, w.seqlen_q, w.seqlen_k, w.causal, heads_k=w.kv_heads)
+              if ws is not None else 1)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)

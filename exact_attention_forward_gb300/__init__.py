@@ -41,7 +41,8 @@ FA_DTYPE_BF16, FA_DTYPE_E4M3, FA_DTYPE_E5M2 = 0, 1, 2
 # Every function declared in include/fa.h.
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_num_splits", "fa_status_string",
                     "fa_last_error_detail", "fa_device_error", "fa_debug_set",
-                    "fa_fwd_static_workspace", "fa_fwd_gqa", "fa_fwd_fp8", "fa_fwd_kvcache")
+                    "fa_fwd_static_workspace", "fa_fwd_gqa", "fa_fwd_fp8", "fa_fwd_kvcache",
+                    "fa_fwd_workspace_size_gqa", "fa_fwd_num_splits_gqa")
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +78,10 @@ def load_library():
         lib.fa_fwd_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.fa_fwd_num_splits.restype = i32
         lib.fa_fwd_num_splits.argtypes = [i32, i32, i32, i32, i32]
+        lib.fa_fwd_workspace_size_gqa.restype = sz
+        lib.fa_fwd_workspace_size_gqa.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+        lib.fa_fwd_num_splits_gqa.restype = i32
+        lib.fa_fwd_num_splits_gqa.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_status_string.argtypes = [i32]
         lib.fa_last_error_detail.restype = ctypes.c_char_p
@@ -113,14 +118,16 @@ def fa_fwd(*args) -> int:
     return load_library().fa_fwd(*args)
 
 
-def workspace_size(batch, heads, seqlen_q, seqlen_k, head_dim_v, causal=False) -> int:
-    return int(load_library().fa_fwd_workspace_size(batch, heads, seqlen_q, seqlen_k, head_dim_v,
-                                                    int(bool(causal))))
+def workspace_size(batch, heads, seqlen_q, seqlen_k, head_dim_v, causal=False, heads_k=None) -> int:
+    return int(load_library().fa_fwd_workspace_size_gqa(
+        batch, heads, heads if heads_k is None else heads_k, seqlen_q, seqlen_k, head_dim_v,
+        int(bool(causal))))
 
 
-def num_splits(batch, heads, seqlen_q, seqlen_k, causal=False) -> int:
-    return int(load_library().fa_fwd_num_splits(batch, heads, seqlen_q, seqlen_k,
-                                                int(bool(causal))))
+def num_splits(batch, heads, seqlen_q, seqlen_k, causal=False, heads_k=None) -> int:
+    return int(load_library().fa_fwd_num_splits_gqa(
+        batch, heads, heads if heads_k is None else heads_k, seqlen_q, seqlen_k,
+        int(bool(causal))))
 
 
 def device_error(clear: bool = True):
@@ -238,7 +245,7 @@ def fwd(q, k, v, *, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
         if workspace != "auto":
             raise ValueError('workspace must be "auto", None or a uint8 CUDA tensor')
         if not varlen:
-            need = workspace_size(batch, heads, sq_arg, sk_arg, dv, causal)
+            need = workspace_size(batch, heads, sq_arg, sk_arg, dv, causal, heads_k=heads_k)
             if need > 0:  # allocated from torch's caching allocator (no cudaMalloc per call)
                 ws = torch.empty(need, dtype=torch.uint8, device=dev)
                 ws_bytes = need
@@ -315,7 +322,7 @@ def fwd_kvcache(q, k_cache, v_cache, cache_seqlens, k_new=None, v_new=None, *, c
         ds, ds_b, ds_h = _fp8_descales(descale, batch, heads_k, dev, temps)
     ws, ws_bytes = None, 0
     if isinstance(workspace, str):
-        need = workspace_size(batch, heads, sq, cap, d, causal) if sq > 0 else 0
+        need = workspace_size(batch, heads, sq, cap, d, causal, heads_k=heads_k) if sq > 0 else 0
         if need > 0:
             ws = torch.empty(need, dtype=torch.uint8, device=dev)
             ws_bytes = need

@@ -8,6 +8,7 @@ library has no load-time dependency on libcuda).
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -35,11 +36,23 @@ def _deps():
 def build(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: str = LIB,
           build_dir: str = BUILD) -> str:
     """Build the library; `extra_flags` / `lib_path` / `build_dir` make a variant build
-    (e.g. a compile-time option) elsewhere without touching the default library."""
-    if (not force and os.path.exists(lib_path)
-            and os.path.getmtime(lib_path) >= max(os.path.getmtime(d) for d in _deps())):
+    (e.g. a compile-time option) elsewhere without touching the default library.
+    Concurrent callers (parallel test workers) serialise on a lock file in build_dir."""
+    def fresh():
+        return (os.path.exists(lib_path)
+                and os.path.getmtime(lib_path) >= max(os.path.getmtime(d) for d in _deps()))
+
+    if not force and fresh():
         return lib_path
     os.makedirs(build_dir, exist_ok=True)
+    with open(os.path.join(build_dir, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and fresh():  # another process built it meanwhile
+            return lib_path
+        return _build_locked(verbose, extra_flags, lib_path, build_dir)
+
+
+def _build_locked(verbose, extra_flags, lib_path, build_dir) -> str:
     nvcc = _nvcc()
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-fvisibility=hidden",

@@ -70,15 +70,17 @@ fa_status device_info(int* dev, int* sms, uint32_t** err) {
 }
 
 // 4-D view (d, head, row, batch) of a [batch, rows, heads, d] tensor; box =
-// one 128-byte swizzle atom of d by 128 rows of one head.
+// one 128-byte swizzle atom of d by 128 rows of one head, or (box_heads > 1) by
+// box_heads heads x 128 / box_heads rows -- 128 shared-memory rows either way.
 fa_status encode_map(CUtensorMap* m, const void* base, bool fp8, int d, int heads, int rows,
-                     int batch) {
+                     int batch, int box_heads = 1) {
     const int elem = fp8 ? 1 : 2;
     cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1),
                           (cuuint64_t)(batch > 0 ? batch : 1)};
     cuuint64_t strides[3] = {(cuuint64_t)d * elem, (cuuint64_t)heads * d * elem,
                              (cuuint64_t)(rows > 0 ? rows : 1) * heads * d * elem};
-    cuuint32_t box[4] = {(cuuint32_t)(128 / elem), 1u, 128u, 1u};
+    cuuint32_t box[4] = {(cuuint32_t)(128 / elem), (cuuint32_t)box_heads,
+                         (cuuint32_t)(128 / box_heads), 1u};
     cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     CUresult r = g_encode(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                           const_cast<void*>(base), dims, strides, box, estr,
@@ -102,6 +104,22 @@ int choose_splits(int batch, int heads, int sq, int sk, int causal, int sms) {
     if (s < 2) return 1;
     const int bps = ceil_div(nblk, s);
     return ceil_div(nblk, bps);
+}
+
+// Grouped-query packing: the query heads that share a K/V head are packed into the
+// rows of one tile (row = query row x head) when a whole group of short query blocks
+// fits one tile pair -- decoding and short prefill chunks, where one head per tile
+// would leave most tile rows empty and stream each K/V head once per query head.
+int choose_pack(int heads, int heads_k, int sq, bool varlen) {
+    const int group = heads / heads_k;
+    if (varlen || group <= 1 || 128 % group != 0 || (long long)sq * group > 256) return 1;
+    return group;
+}
+
+// Splits of the key range for a fixed-length shape, taking packing into account.
+int plan_splits(int batch, int heads, int heads_k, int sq, int sk, int causal, int sms) {
+    const int pack = choose_pack(heads, heads_k, sq, false);
+    return choose_splits(batch, heads / pack, sq * pack, sk, causal, sms);
 }
 
 size_t workspace_bytes_for(int splits, int batch, int heads, int sq, int dv) {
@@ -312,9 +330,10 @@ fa_status fwd_impl(const FwdArgs& a) {
     if (st != FA_OK) return st;
 
     // ---------------------------------------------------------------- decomposition
+    const int pack = choose_pack(a.heads, a.heads_k, mq, varlen);
     int splits = 1;
     if (!varlen && a.workspace && mq > 0) {
-        splits = choose_splits(a.batch, a.heads, a.seqlen_q, a.seqlen_k, a.causal, sms);
+        splits = plan_splits(a.batch, a.heads, a.heads_k, a.seqlen_q, a.seqlen_k, a.causal, sms);
         const size_t need = workspace_bytes_for(splits, a.batch, a.heads, a.seqlen_q, a.head_dim_v);
         if (a.workspace_bytes < need)
             return fail(FA_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed",
@@ -338,14 +357,16 @@ fa_status fwd_impl(const FwdArgs& a) {
     p.batch = a.batch;
     p.heads = a.heads;
     p.kv_group = a.heads / a.heads_k;
+    p.pack = pack;
+    p.item_heads = a.heads / pack;
     p.seqlen_q = mq;
     p.seqlen_k = mk;
     p.total_q = varlen ? a.seqlen_q : 0;
-    p.n_mpairs = ceil_div(mq, 256);
+    p.n_mpairs = ceil_div((long long)mq * pack, 256);
     p.n_splits = splits;
     const int nblk = ceil_div(mk > 0 ? mk : 1, 128);
     p.blocks_per_split = splits > 1 ? ceil_div(nblk, splits) : (1 << 29);
-    const long long n_items = (long long)p.n_mpairs * a.batch * a.heads * splits;
+    const long long n_items = (long long)p.n_mpairs * a.batch * p.item_heads * splits;
     if (n_items >= (1ll << 31)) return fail(FA_ERR_INVALID_ARG, "too many work items");
     p.n_items = (int)n_items;
     p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -368,7 +389,10 @@ fa_status fwd_impl(const FwdArgs& a) {
     CUtensorMap tq, tk, tv;
     // fixed length: (d, head, seq row, batch); varlen: (d, head, packed row, 1)
     const int nbat = varlen ? 1 : a.batch;
-    if ((st = encode_map(&tq, a.q, fp8, a.head_dim, a.heads, a.seqlen_q, nbat)) != FA_OK) return st;
+    // packed: one box spans the group's `pack` heads x 128 / pack rows, which lands in
+    // shared memory as 128 tile rows ordered (query row, head)
+    if ((st = encode_map(&tq, a.q, fp8, a.head_dim, a.heads, a.seqlen_q, nbat, pack)) != FA_OK)
+        return st;
     if (no_keys) {  // no key block is ever loaded; any valid map will do
         tk = tq;
         tv = tq;
@@ -455,19 +479,30 @@ fa_status fa_device_error(uint32_t* flags, int clear) {
     return FA_OK;
 }
 
-int fa_fwd_num_splits(int batch, int heads, int seqlen_q, int seqlen_k, int causal) {
+int fa_fwd_num_splits_gqa(int batch, int heads, int heads_k, int seqlen_q, int seqlen_k,
+                          int causal) {
     int dev, sms;
     uint32_t* err;
     if (batch < 1 || heads < 1 || seqlen_q < 1 || seqlen_k < 1) return 1;
+    if (heads_k < 1 || heads % heads_k != 0) return 1;
     if (device_info(&dev, &sms, &err) != FA_OK) return 1;
-    return choose_splits(batch, heads, seqlen_q, seqlen_k, causal, sms);
+    return plan_splits(batch, heads, heads_k, seqlen_q, seqlen_k, causal, sms);
+}
+
+int fa_fwd_num_splits(int batch, int heads, int seqlen_q, int seqlen_k, int causal) {
+    return fa_fwd_num_splits_gqa(batch, heads, heads, seqlen_q, seqlen_k, causal);
+}
+
+size_t fa_fwd_workspace_size_gqa(int batch, int heads, int heads_k, int seqlen_q, int seqlen_k,
+                                 int head_dim_v, int causal) {
+    const int s = fa_fwd_num_splits_gqa(batch, heads, heads_k, seqlen_q, seqlen_k, causal);
+    if (head_dim_v < 1) return 0;
+    return workspace_bytes_for(s, batch, heads, seqlen_q, head_dim_v);
 }
 
 size_t fa_fwd_workspace_size(int batch, int heads, int seqlen_q, int seqlen_k, int head_dim_v,
                              int causal) {
-    const int s = fa_fwd_num_splits(batch, heads, seqlen_q, seqlen_k, causal);
-    if (head_dim_v < 1) return 0;
-    return workspace_bytes_for(s, batch, heads, seqlen_q, head_dim_v);
+    return fa_fwd_workspace_size_gqa(batch, heads, heads, seqlen_q, seqlen_k, head_dim_v, causal);
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int batch,

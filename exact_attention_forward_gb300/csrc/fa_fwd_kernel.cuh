@@ -29,6 +29,9 @@
 //       warps 8-11  the same for query tile 1
 //   * a work item is (batch, head, 256 query rows = two 128-row tiles, key
 //     split); both tiles consume every K/V block loaded, halving K/V traffic;
+//     for short query blocks of grouped-query attention an item is (batch, K/V
+//     head, ...) and the group's query heads share the tile rows (row = query
+//     row x head), so a K/V block is streamed once per K/V head;
 //   * S_t = Q_t K^T and O_t += P_t V are tcgen05.mma (M=128) with fp32
 //     accumulators in TMEM: S_t at columns [128t, 128t+128), O_t at
 //     [256+128t, 256+128t+Dv); P_t (bf16 or e4m3) is written back over the
@@ -143,13 +146,17 @@ struct Item {
 // they stream the same K/V at about the same time and share it in L2.
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int w) {
     Item it;
-    const int per_m = p.batch * p.heads * p.n_splits;
+    // packed grouped-query mode (p.pack = G > 1): an item serves one K/V head, and its
+    // tile rows are (query row, query head of the group) pairs, row-major: packed row
+    // r = i * G + g.  it.h is then the group's first query head.
+    const int G = p.pack;
+    const int per_m = p.batch * p.item_heads * p.n_splits;
     const int mp = p.n_mpairs - 1 - w / per_m;
     const int r = w % per_m;
     it.split = r % p.n_splits;
     const int bh = r / p.n_splits;
-    it.h = bh % p.heads;
-    it.b = bh / p.heads;
+    it.h = (bh % p.item_heads) * G;
+    it.b = bh / p.item_heads;
     if (p.varlen) {
         it.q_row0 = __ldg(p.cu_q + it.b);
         it.sq = __ldg(p.cu_q + it.b + 1) - it.q_row0;
@@ -173,11 +180,11 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int w) {
     it.n_hi = it.n_lo;
 #pragma unroll
     for (int t = 0; t < kTiles; ++t) {
-        it.m0[t] = mp * (kTiles * kBM) + t * kBM;
-        it.active[t] = it.m0[t] < it.sq;
+        it.m0[t] = mp * (kTiles * kBM) + t * kBM;  // first (packed) row of the tile
+        it.active[t] = it.m0[t] < it.sq * G;
         int hi = n_end;
         if (p.causal) {
-            const int rmax = min(it.m0[t] + kBM, it.sq) - 1;
+            const int rmax = (min(it.m0[t] + kBM, it.sq * G) - 1) / G;  // last query row
             const int last = rmax + it.sk - it.sq;  // last visible key of the tile's last row
             hi = last < 0 ? 0 : min(hi, last / kBN + 1);
         }
@@ -308,7 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         withheld = true;
                         return true;
                     }
-                    const int qrow = (p.varlen ? it.q_row0 : 0) + it.m0[t];
+                    // packed mode: the map's box spans G heads x 128/G rows
+                    const int qrow = (p.varlen ? it.q_row0 : 0) + it.m0[t] / p.pack;
                     mbar_arrive_expect_tx(bar(C::Q_FULL + t), C::kTileBytes);
 #pragma unroll
                     for (int c = 0; c < C::kChunks; ++c)
@@ -532,25 +540,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 scale_log2 *= qd * kd;
                 o_scale = p.v_descale ? __ldg(p.v_descale + ds) : 1.0f;
             }
-            const int row = t_m0 + r_in_tile;  // row within the sequence
-            const bool row_ok = row < it.sq;
+            const int prow = t_m0 + r_in_tile;          // this thread's (packed) tile row
+            const int row = prow / p.pack;               // query row within the sequence
+            const int hrow = it.h + prow % p.pack;       // query head of this row
+            const bool row_ok = prow < it.sq * p.pack;
             // output addresses
             float* lse_ptr;
             float* wso_ptr = nullptr;
             __nv_bfloat16* o_ptr = nullptr;
             if (p.split) {
                 const size_t rid =
-                    (((size_t)it.split * p.batch + it.b) * p.heads + it.h) * (size_t)p.seqlen_q + row;
+                    (((size_t)it.split * p.batch + it.b) * p.heads + hrow) * (size_t)p.seqlen_q + row;
                 lse_ptr = p.ws_lse + rid;
                 wso_ptr = p.ws_o + rid * D;
             } else if (p.varlen) {
-                lse_ptr = p.lse + (size_t)it.h * p.total_q + it.q_row0 + row;
+                lse_ptr = p.lse + (size_t)hrow * p.total_q + it.q_row0 + row;
                 o_ptr = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                        (((size_t)it.q_row0 + row) * p.heads + it.h) * D;
+                        (((size_t)it.q_row0 + row) * p.heads + hrow) * D;
             } else {
-                lse_ptr = p.lse + ((size_t)it.b * p.heads + it.h) * p.seqlen_q + row;
+                lse_ptr = p.lse + ((size_t)it.b * p.heads + hrow) * p.seqlen_q + row;
                 o_ptr = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                        (((size_t)it.b * p.seqlen_q + row) * p.heads + it.h) * D;
+                        (((size_t)it.b * p.seqlen_q + row) * p.heads + hrow) * D;
             }
             if (t_hi <= it.n_lo) {
                 // no visible key for any row of this tile: O = 0, LSE = -inf
@@ -569,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // visible keys of this row: [0, vis_end) with vis_end = min(sk, row + sk - sq + 1)
             const int vis_end = p.causal ? min(it.sk, row + it.sk - it.sq + 1) : it.sk;
             // a block needs masking iff some column of it is invisible to some row of the tile
-            const int tile_rmin = t_m0;
+            const int tile_rmin = t_m0 / p.pack;  // the tile's first query row
             const int tile_vis_min = p.causal ? min(it.sk, tile_rmin + it.sk - it.sq + 1) : it.sk;
             float m_run = -INFINITY;  // running max of scale_log2 * s (lazy reference)
             float l_run = 0.0f;       // running sum of exp2(scale_log2 * s - m_run)

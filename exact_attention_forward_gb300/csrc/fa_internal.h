@@ -27,12 +27,15 @@ struct FwdParams {
     uint32_t* err;              // device error word
     int batch, heads;
     int kv_group;               // query heads per K/V head (grouped-query attention; 1 = MHA)
+    int pack;                   // > 1: the kv_group query heads of a K/V head share tiles
+                                //   (rows = query row x head); 1: one head per tile
+    int item_heads;             // heads the items run over: heads, or heads / pack
     int seqlen_q, seqlen_k;     // fixed length: the lengths; varlen: max lengths
     int total_q;                // varlen: packed rows of Q (LSE row stride)
-    int n_mpairs;               // ceil(seqlen_q / 256): query-row pairs of tiles
+    int n_mpairs;               // ceil(seqlen_q * pack / 256): (packed) row pairs of tiles
     int n_splits;               // key-range splits (1 = none)
     int blocks_per_split;       // key blocks per split
-    int n_items;                // n_mpairs * batch * heads * n_splits
+    int n_items;                // n_mpairs * batch * item_heads * n_splits
     float scale_log2;           // softmax_scale * log2(e)
     int causal, varlen, split;
     int v_e5m2;                 // FP8: V stored as E5M2 (Q, K and P stay E4M3)

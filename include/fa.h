@@ -180,7 +180,8 @@ FA_API fa_status fa_fwd_fp8(const void* q, const void* k, const void* v,
  * rows appended, its attention uses the length clamped to [0, capacity], and
  * fa_device_error() afterwards returns FA_ERR_DEVICE_ARG.  workspace: as fa_fwd
  * (key splits for short-query / long-cache shapes, sized by
- * fa_fwd_workspace_size(batch, heads, seqlen_q, cache_capacity, head_dim, causal)).
+ * fa_fwd_workspace_size_gqa(batch, heads, heads_k, seqlen_q, cache_capacity,
+ * head_dim, causal)).
  */
 FA_API fa_status fa_fwd_kvcache(const void* q, void* k_cache, void* v_cache,
                                 const void* k_new, const void* v_new,
@@ -207,6 +208,19 @@ FA_API size_t fa_fwd_workspace_size(int batch, int heads, int seqlen_q, int seql
 
 /* Number of key splits fa_fwd would use for that shape with a workspace. */
 FA_API int fa_fwd_num_splits(int batch, int heads, int seqlen_q, int seqlen_k, int causal);
+
+/*
+ * The same two queries for grouped-query shapes (heads_k K/V heads; fa_fwd_gqa,
+ * fa_fwd_fp8, fa_fwd_kvcache with cache_capacity as seqlen_k).  When a whole group of
+ * short query blocks fits one 256-row tile pair (heads / heads_k a power of two
+ * <= 128 and seqlen_q * heads / heads_k <= 256, fixed length), the query heads of a
+ * group share tiles, so fewer work items exist and more key splits may be used; the
+ * MHA queries above then under-size the workspace (FA_ERR_WORKSPACE).
+ */
+FA_API size_t fa_fwd_workspace_size_gqa(int batch, int heads, int heads_k, int seqlen_q,
+                                        int seqlen_k, int head_dim_v, int causal);
+FA_API int fa_fwd_num_splits_gqa(int batch, int heads, int heads_k, int seqlen_q, int seqlen_k,
+                                 int causal);
 
 /*
  * fa_fwd_static_workspace -- fa_fwd for fixed-length inputs, for callers that

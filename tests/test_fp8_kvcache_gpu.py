@@ -49,6 +49,7 @@ def _fp8_head_inputs(B, H, Hk, Sq, Sk, v_dtype, seed):
     (2, 4, 2, 300, 400, True, "e5m2"),
     (3, 6, 3, 129, 257, True, "e4m3"),     # per-head descales with an E4M3 V
     (1, 8, 1, 128, 3000, False, "e5m2"),   # multi-query; splits the key range
+    (2, 8, 2, 50, 600, True, "e5m2"),      # group 4 x 50 rows: heads share tiles
 ])
 def test_fp8_head_descales_full(B, H, Hk, Sq, Sk, causal, v_dtype):
     x = _fp8_head_inputs(B, H, Hk, Sq, Sk, v_dtype, seed=200 + H + Hk + Sq)

@@ -190,6 +190,24 @@ def test_grouped_query_full(B, H, Hk, Sq, Sk, D, causal):
     compare(o, lse, o_ref, lse_ref, what=f"gqa {(B, H, Hk, Sq, Sk, D, causal)}")
 
 
+@pytest.mark.parametrize("B,H,Hk,Sq,Sk,D,causal", [
+    (2, 8, 2, 64, 700, 128, True),       # group 4 x 64 rows: one full tile pair
+    (1, 32, 4, 7, 1000, 128, True),      # group 8 x 7 rows: part of tile 0
+    (3, 6, 3, 100, 300, 128, True),      # group 2 x 100 rows: tile 1 partly filled
+    (1, 16, 1, 16, 5000, 128, False),    # multi-query, 16 heads x 16 rows, key splits
+    (2, 8, 2, 32, 500, 64, True),        # D = 64
+    (1, 6, 2, 10, 300, 128, True),       # group 3 does not divide 128: not packed
+    (2, 4, 2, 1, 2000, 128, True),       # decoding: one query row
+])
+def test_grouped_query_packed_tiles(B, H, Hk, Sq, Sk, D, causal):
+    # short query blocks: the query heads of a K/V head share the rows of one tile
+    x = inputs.make_random(B, H, Sq, Sk, D, seed=120 + H + Hk + Sq + D, heads_k=Hk)
+    o, lse = run_gpu(x, causal=causal, softmax_scale=D ** -0.5)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=D ** -0.5,
+                                      causal=causal)
+    compare(o, lse, o_ref, lse_ref, what=f"packed gqa {(B, H, Hk, Sq, Sk, D, causal)}")
+
+
 def test_grouped_query_varlen_and_fp8():
     x = inputs.make_varlen([40, 300, 0, 129], [40, 300, 5, 200], heads=4, head_dim=128, seed=95,
                            heads_k=2)
