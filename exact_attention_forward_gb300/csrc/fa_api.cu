@@ -403,6 +403,11 @@ fa_status fwd_impl(const FwdArgs& a) {
             return st;
     }
 
+    // O (bf16) is stored by TMA from 128-row staging tiles: the same 4-D view and box as Q
+    CUtensorMap to;
+    if ((st = encode_map(&to, a.o, false, a.head_dim_v, a.heads, a.seqlen_q, nbat, pack)) != FA_OK)
+        return st;
+
     // ---------------------------------------------------------------- launches
     cudaStream_t s = static_cast<cudaStream_t>(a.stream);
     cudaError_t e;
@@ -415,11 +420,11 @@ fa_status fwd_impl(const FwdArgs& a) {
     if (rows_q == 0 || mq == 0) return FA_OK;
     const int grid = (int)(n_items < sms ? n_items : sms);
     if (fp8)
-        e = launch_fwd_e4m3_d128(tq, tk, tv, p, grid, s);
+        e = launch_fwd_e4m3_d128(tq, tk, tv, to, p, grid, s);
     else if (a.head_dim == 64)
-        e = launch_fwd_bf16_d64(tq, tk, tv, p, grid, s);
+        e = launch_fwd_bf16_d64(tq, tk, tv, to, p, grid, s);
     else
-        e = launch_fwd_bf16_d128(tq, tk, tv, p, grid, s);
+        e = launch_fwd_bf16_d128(tq, tk, tv, to, p, grid, s);
     if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
     if (p.split) {
         e = launch_combine(p.ws_o, p.ws_lse, a.o, a.lse, a.batch, a.heads, a.seqlen_q,

@@ -3,7 +3,8 @@
 
 namespace fa {
 cudaError_t launch_fwd_bf16_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const CUtensorMap& o,
                           const FwdParams& p, int grid, cudaStream_t s) {
-    return launch_fwd<64, false>(q, k, v, p, grid, s);
+    return launch_fwd<64, false>(q, k, v, o, p, grid, s);
 }
 }  // namespace fa

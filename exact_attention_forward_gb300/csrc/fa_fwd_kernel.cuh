@@ -110,10 +110,14 @@ struct Cfg {
     static constexpr int kPCols = kBN * kElem / 4;         // TMEM columns of a P tile
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = kTiles * kTileBytes;
-    static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+    // epilogue staging: per tile, 128 rows x 64 bf16 columns of O (one 128-byte swizzle atom
+    // wide), stored to HBM by TMA; a D = 128 tile goes out in two halves
+    static constexpr int kStageBytes = kBM * 128;
+    static constexpr int kStageOff = kKVOff + kStages * kTileBytes;
+    static constexpr int kBarOff = kStageOff + kTiles * kStageBytes;
     enum {
-        Q_FULL = 0, Q_EMPTY = 2, S_FULL = 4, P_FULL = 6, O_FULL = 8, O_EMPTY = 10, DRAIN = 12,
-        KV_FULL = 13, KV_EMPTY = 13 + kStages, NUM_BARS = 13 + 2 * kStages
+        Q_FULL = 0, Q_EMPTY = 2, S_FULL = 4, P_FULL = 6, O_FULL = 8, O_EMPTY = 10, STG_FULL = 12,
+        STG_EMPTY = 14, DRAIN = 16, KV_FULL = 17, KV_EMPTY = 17 + kStages, NUM_BARS = 17 + 2 * kStages
     };
     static constexpr int kMiscOff = kBarOff + NUM_BARS * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1 KiB
@@ -235,13 +239,15 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
 // Wait-site codes reported in bits 8..15 of the error word.
 enum : uint32_t {
     SITE_Q_EMPTY = 1, SITE_KV_EMPTY = 2, SITE_Q_FULL = 3, SITE_KV_FULL = 4, SITE_P_FULL = 5,
-    SITE_O_EMPTY = 6, SITE_S_FULL = 7, SITE_O_FULL = 8, SITE_DRAIN = 9
+    SITE_O_EMPTY = 6, SITE_S_FULL = 7, SITE_O_FULL = 8, SITE_DRAIN = 9, SITE_STG_FULL = 10,
+    SITE_STG_EMPTY = 11
 };
 
 template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const FwdParams p) {
     using C = Cfg<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -265,6 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::P_FULL + t), kBM / 32);   // one arrival per softmax warp
             mbar_init(bar(C::O_FULL + t), 1);
             mbar_init(bar(C::O_EMPTY + t), kBM / 32);
+            mbar_init(bar(C::STG_FULL + t), kBM / 32);  // every warp of the tile wrote its rows
+            mbar_init(bar(C::STG_EMPTY + t), 1);        // the store has read the staging rows
         }
         mbar_init(bar(C::DRAIN), 1);
         for (int s = 0; s < C::kStages; ++s) {
@@ -294,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_o);
             const uint64_t pol_q = l2_policy_evict_first();
             const uint64_t pol_kv = l2_policy_evict_last();
             uint32_t ring = 0, ph_qe = 0;  // bit t: parity of the last Q_EMPTY wait of tile t
@@ -511,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t t_s = t_lane + 128u * t;     // S_t (fp32) and, over it, P_t
         const uint32_t t_o = t_lane + C::kColO + 128u * t;
         uint32_t s_cnt = 0, o_cnt = 0;
+        uint32_t stg_cnt = 0;  // staging-buffer passes of this tile so far (both barriers' phase)
         uint32_t kv_base = 0;  // ring position of the current item's first K/V load
         const bool releaser = wq == 0 && lane == 0;  // this warpgroup's slot-release thread
         bool aborted = false;
@@ -737,28 +747,82 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (releaser) mbar_arrive(bar(C::KV_EMPTY + v_slot(it.n_lo)));  // PV_t(n_lo) is complete
             const bool has_mass = l_run > 0.0f;
             const float inv_l = has_mass ? o_scale / l_run : 0.0f;
+            // The O tile goes out by TMA store from a per-tile staging buffer (128 rows x 64
+            // columns, 128-byte swizzled like the tensor map), in D / 64 passes.  Rows past a
+            // fixed-length sequence's end fall outside the map and are clipped; a varlen tile
+            // that crosses its sequence's end (the next rows belong to another sequence) and
+            // the fp32 split partials use plain stores instead.
+            const bool use_tma = !p.split && (!p.varlen || t_m0 + kBM <= it.sq * p.pack);
+            if (use_tma) {
+                const uint32_t srow = s_base + C::kStageOff + (uint32_t)t * C::kStageBytes +
+                                      (uint32_t)r_in_tile * 128u;
+                const uint32_t sw = (uint32_t)(r_in_tile & 7);
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                uint32_t orr[32];
-                tmem_ld32(t_o + c, orr);
-                tmem_wait_ld();
-                if (row_ok) {
-                    if (p.split) {
+                for (int hh = 0; hh < D / 64; ++hh) {
+                    // the previous store out of this buffer has read it
+                    if (stg_cnt > 0 &&
+                        !wait_bar(bar(C::STG_EMPTY + t), (stg_cnt - 1) & 1u, wc, SITE_STG_EMPTY)) {
+                        aborted = true;
+                    }
+                    if (__any_sync(0xffffffffu, aborted)) break;
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4*>(wso_ptr + c + i) = make_float4(
-                                __uint_as_float(orr[i]) * inv_l, __uint_as_float(orr[i + 1]) * inv_l,
-                                __uint_as_float(orr[i + 2]) * inv_l, __uint_as_float(orr[i + 3]) * inv_l);
-                    } else {
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        uint32_t orr[32];
+                        tmem_ld32(t_o + hh * 64 + c2 * 32, orr);
+                        tmem_wait_ld();
                         uint32_t pk[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             pk[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
                                                 __uint_as_float(orr[2 * i + 1]) * inv_l);
+                        // 16-byte chunk c of the row lands at chunk c ^ (row mod 8)
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            *reinterpret_cast<uint4*>(o_ptr + c + 8 * i) =
-                                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            st_shared_v4(srow + ((((uint32_t)(c2 * 4 + k4)) ^ sw) << 4), pk[4 * k4],
+                                         pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
+                    }
+                    fence_proxy_async_smem();  // generic-proxy writes -> visible to the TMA engine
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::STG_FULL + t));
+                    if (r_in_tile == 0) {
+                        if (wait_bar(bar(C::STG_FULL + t), stg_cnt & 1u, wc, SITE_STG_FULL)) {
+                            tma_store_4d(&tm_o, s_base + C::kStageOff + (uint32_t)t * C::kStageBytes,
+                                         hh * 64, it.h, (p.varlen ? it.q_row0 : 0) + t_m0 / p.pack,
+                                         p.varlen ? 0 : it.b);
+                            bulk_commit_group();
+                            bulk_wait_group_read0();
+                            mbar_arrive(bar(C::STG_EMPTY + t));
+                        } else {
+                            aborted = true;
+                        }
+                    }
+                    ++stg_cnt;
+                }
+                if (__any_sync(0xffffffffu, aborted)) break;
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t orr[32];
+                    tmem_ld32(t_o + c, orr);
+                    tmem_wait_ld();
+                    if (row_ok) {
+                        if (p.split) {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4)
+                                *reinterpret_cast<float4*>(wso_ptr + c + i) = make_float4(
+                                    __uint_as_float(orr[i]) * inv_l, __uint_as_float(orr[i + 1]) * inv_l,
+                                    __uint_as_float(orr[i + 2]) * inv_l, __uint_as_float(orr[i + 3]) * inv_l);
+                        } else {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                pk[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
+                                                    __uint_as_float(orr[2 * i + 1]) * inv_l);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                *reinterpret_cast<uint4*>(o_ptr + c + 8 * i) =
+                                    make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        }
                     }
                 }
             }
@@ -770,6 +834,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    // the TMA stores of O have completed before this CTA retires (their issuing threads wait)
+    if (warp >= 4 && (threadIdx.x & (kBM - 1)) == 0) bulk_wait_group0();
     __syncthreads();
     // lets a programmatically dependent grid (the split merge) be scheduled; it still
     // waits for this grid's completion before reading anything
@@ -783,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool FP8>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                       const FwdParams& p, int grid, cudaStream_t stream) {
+                       const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t stream) {
     using C = Cfg<D, FP8>;
     static bool attr_done = false;  // per process; the attribute is per function
     if (!attr_done) {
@@ -793,7 +859,7 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    fa_fwd_kernel<D, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, p);
+    fa_fwd_kernel<D, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, o, p);
     return cudaGetLastError();
 }
 
