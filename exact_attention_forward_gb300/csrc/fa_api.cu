@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include <cuda_bf16.h>
@@ -18,6 +19,12 @@ namespace fa {
 
 __device__ uint32_t g_fa_error_word;
 
+// Work counters of the greedy item scheduler (varlen launches): one {next item, CTAs
+// done} pair per launch slot.  Each launch takes the next slot round-robin and its last CTA returns the
+// pair to zero, so up to kSchedSlots launches may be in flight on a device at once.
+constexpr int kSchedSlots = 256;
+__device__ uint32_t g_fa_sched[2 * kSchedSlots];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -29,6 +36,8 @@ uint64_t g_wait_limit_ns = kDefaultWaitNs;
 uint32_t g_inject = 0;
 int g_num_sms[kMaxDevices] = {0};
 uint32_t* g_err_addr[kMaxDevices] = {nullptr};
+uint32_t* g_sched_addr[kMaxDevices] = {nullptr};
+std::atomic<uint32_t> g_sched_next{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 fa_status fail(fa_status s, const char* fmt, ...) {
@@ -54,6 +63,9 @@ fa_status device_info(int* dev, int* sms, uint32_t** err) {
         e = cudaGetSymbolAddress(&addr, g_fa_error_word);
         if (e != cudaSuccess) return fail(FA_ERR_CUDA, "error word: %s", cudaGetErrorString(e));
         g_err_addr[*dev] = static_cast<uint32_t*>(addr);
+        e = cudaGetSymbolAddress(&addr, g_fa_sched);
+        if (e != cudaSuccess) return fail(FA_ERR_CUDA, "work counters: %s", cudaGetErrorString(e));
+        g_sched_addr[*dev] = static_cast<uint32_t*>(addr);
         g_num_sms[*dev] = n;
     }
     if (!g_encode) {
@@ -67,6 +79,11 @@ fa_status device_info(int* dev, int* sms, uint32_t** err) {
     *sms = g_num_sms[*dev];
     *err = g_err_addr[*dev];
     return FA_OK;
+}
+
+uint32_t* next_sched_slot(int dev) {
+    const uint32_t slot = g_sched_next.fetch_add(1u) % (uint32_t)kSchedSlots;
+    return g_sched_addr[dev] + 2 * slot;
 }
 
 // 4-D view (d, head, row, batch) of a [batch, rows, heads, d] tensor; box =
@@ -354,6 +371,7 @@ fa_status fwd_impl(const FwdArgs& a) {
     p.seqused_k = a.seqused_k;
     p.seqused_add = a.seqused_add;
     p.err = err;
+    p.sched = next_sched_slot(dev);
     p.batch = a.batch;
     p.heads = a.heads;
     p.kv_group = a.heads / a.heads_k;
@@ -372,6 +390,7 @@ fa_status fwd_impl(const FwdArgs& a) {
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.causal = a.causal;
     p.varlen = varlen ? 1 : 0;
+    p.greedy = varlen ? 1 : 0;  // varlen item costs are unknown on the host
     p.split = splits > 1 ? 1 : 0;
     p.v_e5m2 = a.v_dtype == FA_DTYPE_E5M2 ? 1 : 0;
     if (p.split) {

@@ -117,7 +117,8 @@ struct Cfg {
     static constexpr int kBarOff = kStageOff + kTiles * kStageBytes;
     enum {
         Q_FULL = 0, Q_EMPTY = 2, S_FULL = 4, P_FULL = 6, O_FULL = 8, O_EMPTY = 10, STG_FULL = 12,
-        STG_EMPTY = 14, DRAIN = 16, KV_FULL = 17, KV_EMPTY = 17 + kStages, NUM_BARS = 17 + 2 * kStages
+        STG_EMPTY = 14, ITEM_FULL = 16, ITEM_EMPTY = 18, DRAIN = 20, KV_FULL = 21,
+        KV_EMPTY = 21 + kStages, NUM_BARS = 21 + 2 * kStages
     };
     static constexpr int kMiscOff = kBarOff + NUM_BARS * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1 KiB
@@ -199,9 +200,17 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int w) {
     return it;
 }
 
-// Snake-ordered static assignment of items to persistent CTAs: round r hands
-// items [r*G, (r+1)*G) to the CTAs in forward order on even rounds and in
-// reverse order on odd ones, which balances the descending item costs.
+// Which item a CTA takes next is decided by its producer thread, which passes the
+// index to the MMA issuer and the softmax warps through a two-entry ring in shared
+// memory (ITEM_FULL / ITEM_EMPTY mbarriers), published once the current item's loads
+// are issued -- before the current item's epilogue.  CTA c starts with item c; then
+//  * fixed length (item costs known from the index): a static snake -- round r hands
+//    items [r*G, (r+1)*G) to the CTAs in forward order on even rounds and in reverse
+//    order on odd ones, which balances the descending item costs;
+//  * varlen (costs depend on lengths that live on the device): greedy -- the next index
+//    comes from a device-wide counter (atomicAdd), so a CTA that finishes early takes
+//    the next (in LPT order: the next most expensive) item.
+constexpr uint32_t kItemConsumers = 1 + 2 * (kBM / 32);  // issuer + one arrival per softmax warp
 __device__ __forceinline__ int item_of_round(int round, int nctas) {
     const int pos = (round & 1) ? (nctas - 1 - (int)blockIdx.x) : (int)blockIdx.x;
     return round * nctas + pos;
@@ -240,7 +249,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
 enum : uint32_t {
     SITE_Q_EMPTY = 1, SITE_KV_EMPTY = 2, SITE_Q_FULL = 3, SITE_KV_FULL = 4, SITE_P_FULL = 5,
     SITE_O_EMPTY = 6, SITE_S_FULL = 7, SITE_O_FULL = 8, SITE_DRAIN = 9, SITE_STG_FULL = 10,
-    SITE_STG_EMPTY = 11
+    SITE_STG_EMPTY = 11, SITE_ITEM_FULL = 12, SITE_ITEM_EMPTY = 13
 };
 
 template <int D, bool FP8>
@@ -258,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_bar = s_base + C::kBarOff;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
+    volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 8);  // 2 entries
     auto bar = [&](int i) -> uint32_t { return s_bar + 8u * (uint32_t)i; };
 
     const int warp = threadIdx.x >> 5;
@@ -275,6 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::STG_EMPTY + t), 1);        // the store has read the staging rows
         }
         mbar_init(bar(C::DRAIN), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(C::ITEM_FULL + i), 1);
+            mbar_init(bar(C::ITEM_EMPTY + i), kItemConsumers);
+        }
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar(C::KV_FULL + s), 1);
             mbar_init(bar(C::KV_EMPTY + s), kTiles);  // one release per query tile
@@ -292,7 +306,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtx wc{p.wait_limit_ns, p.err, abort_flag};
-    const int nctas = (int)gridDim.x;
+    // consumer side of the item ring: the next item index (n_items = no more work)
+    uint32_t items_read = 0;
+    auto read_item = [&](int& w) -> bool {
+        const uint32_t slot = items_read & 1u;
+        if (!wait_bar(bar(C::ITEM_FULL + slot), (items_read >> 1) & 1u, wc, SITE_ITEM_FULL)) return false;
+        w = item_ring[slot];
+        ++items_read;
+        return true;
+    };
 
     if (warp < 4) {
     setmaxnreg_dec<kRegsLoadMma>();
@@ -308,11 +330,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ring = 0, ph_qe = 0;  // bit t: parity of the last Q_EMPTY wait of tile t
             bool withheld = false;
             bool aborted = false;
-            for (int round = 0; !aborted; ++round) {
-                const int w = item_of_round(round, nctas);
-                if (w >= p.n_items) break;
+            uint32_t published = 0;
+            auto publish = [&](int w) -> bool {
+                const uint32_t slot = published & 1u;
+                if (published >= 2 &&
+                    !wait_bar(bar(C::ITEM_EMPTY + slot), ((published >> 1) - 1) & 1u, wc, SITE_ITEM_EMPTY))
+                    return false;
+                item_ring[slot] = w;
+                mbar_arrive(bar(C::ITEM_FULL + slot));  // release: the index is visible to waiters
+                ++published;
+                return true;
+            };
+            // Every CTA counts itself once when it will fetch no more (its last fetch, or an
+            // abort); the last one returns the counter pair to zero for the next launch that
+            // uses it -- by then no CTA of this launch touches the counter again.
+            bool counted = false;
+            auto fetching_done = [&]() {
+                if (counted) return;
+                counted = true;
+                if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+                    p.sched[0] = 0u;
+                    p.sched[1] = 0u;
+                }
+            };
+            int w_next = (int)blockIdx.x;
+            int round_no = 0;  // static order: rounds of the snake
+            if (!publish(w_next)) aborted = true;
+            for (int w = w_next; !aborted && w < p.n_items; w = w_next) {
+                // the next index is requested now and published once this item's loads have
+                // been issued, so the counter's round trip overlaps them
+                ++round_no;
+                const uint32_t ticket = p.greedy ? atomicAdd(p.sched, 1u) : 0u;
                 const Item it = decode_item(p, w);
-                if (it.n_hi <= it.n_lo) continue;
                 const int bc = p.varlen ? 0 : it.b;  // batch coordinate of the 4-D view
                 auto load_q = [&](auto tc) -> bool {
                     constexpr int t = decltype(tc)::value;
@@ -333,12 +382,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     bar(C::Q_FULL + t), c * C::kChunkElems, it.h, qrow, bc, pol_q);
                     return true;
                 };
-                if (!load_q(std::integral_constant<int, 0>{}) || !load_q(std::integral_constant<int, 1>{})) {
+                const bool has_work = it.n_hi > it.n_lo;
+                if (has_work &&
+                    (!load_q(std::integral_constant<int, 0>{}) || !load_q(std::integral_constant<int, 1>{}))) {
                     aborted = true;
                     break;
                 }
                 const int kv_head = it.h / p.kv_group;  // grouped-query: shared K/V head
-                for (int j = it.n_hi - 1; j >= it.n_lo && !aborted; --j) {
+                for (int j = has_work ? it.n_hi - 1 : it.n_lo - 1; j >= it.n_lo && !aborted; --j) {
                     const int krow = (p.varlen ? it.k_row0 : 0) + j * kBN;
 #pragma unroll
                     for (int kv = 0; kv < 2; ++kv) {
@@ -357,7 +408,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++ring;
                     }
                 }
+                if (aborted) break;
+                if (p.greedy) {
+                    w_next = min((int)(gridDim.x + ticket), p.n_items);
+                    if (w_next >= p.n_items) fetching_done();
+                } else {
+                    w_next = min(item_of_round(round_no, (int)gridDim.x), p.n_items);
+                }
+                if (!publish(w_next)) {
+                    aborted = true;
+                    break;
+                }
             }
+            if (p.greedy) fetching_done();  // after an abort, or with no item beyond the first
             if (aborted) {  // let copies already in flight land before the CTA retires
                 const uint64_t t0 = globaltimer_ns();
                 while (globaltimer_ns() - t0 < 200000ull) {
@@ -416,8 +479,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     kk > 0 ? 1u : acc);
                 }
             };
-            for (int round = 0; !aborted; ++round) {
-                const int w = item_of_round(round, nctas);
+            for (;;) {
+                int w;
+                if (!read_item(w)) {
+                    aborted = true;
+                    break;
+                }
+                mbar_arrive(bar(C::ITEM_EMPTY + ((items_read - 1) & 1u)));
                 if (w >= p.n_items) break;
                 const Item it = decode_item(p, w);
                 if (it.n_hi <= it.n_lo) continue;
@@ -524,8 +592,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t kv_base = 0;  // ring position of the current item's first K/V load
         const bool releaser = wq == 0 && lane == 0;  // this warpgroup's slot-release thread
         bool aborted = false;
-        for (int round = 0; !aborted; ++round) {
-            const int w = item_of_round(round, nctas);
+        for (;;) {
+            int w = 0;
+            bool got = read_item(w);
+            got = __all_sync(0xffffffffu, got);
+            if (!got) {
+                aborted = true;
+                break;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::ITEM_EMPTY + ((items_read - 1) & 1u)));
             if (w >= p.n_items) break;
             const Item it = decode_item(p, w);
             if (it.bad_len && r_in_tile == 0 && t == 0) atomicOr(p.err, kErrBadLength);

@@ -25,6 +25,7 @@ struct FwdParams {
     float* ws_o;                // split mode: normalised partial O [splits, B, H, Sq, Dv] fp32
     float* ws_lse;              // split mode: partial LSE [splits, B, H, Sq] fp32
     uint32_t* err;              // device error word
+    uint32_t* sched;            // work counter pair {next item - grid, CTAs done}, zero at launch
     int batch, heads;
     int kv_group;               // query heads per K/V head (grouped-query attention; 1 = MHA)
     int pack;                   // > 1: the kv_group query heads of a K/V head share tiles
@@ -38,6 +39,7 @@ struct FwdParams {
     int n_items;                // n_mpairs * batch * item_heads * n_splits
     float scale_log2;           // softmax_scale * log2(e)
     int causal, varlen, split;
+    int greedy;                 // items handed out by the device counter (varlen) or a static snake
     int v_e5m2;                 // FP8: V stored as E5M2 (Q, K and P stay E4M3)
     uint64_t wait_limit_ns;     // bound of every device-side wait
     uint32_t inject;            // debug fault injection (see fa_debug_set)
