@@ -439,11 +439,11 @@ fa_status fwd_impl(const FwdArgs& a) {
     if (rows_q == 0 || mq == 0) return FA_OK;
     const int grid = (int)(n_items < sms ? n_items : sms);
     if (fp8)
-        e = launch_fwd_e4m3_d128(tq, tk, tv, to, p, grid, s);
+        e = launch_fwd_e4m3_d128(tq, tk, tv, to, p, grid, s, append);
     else if (a.head_dim == 64)
-        e = launch_fwd_bf16_d64(tq, tk, tv, to, p, grid, s);
+        e = launch_fwd_bf16_d64(tq, tk, tv, to, p, grid, s, append);
     else
-        e = launch_fwd_bf16_d128(tq, tk, tv, to, p, grid, s);
+        e = launch_fwd_bf16_d128(tq, tk, tv, to, p, grid, s, append);
     if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
     if (p.split) {
         e = launch_combine(p.ws_o, p.ws_lse, a.o, a.lse, a.batch, a.heads, a.seqlen_q,

@@ -20,6 +20,9 @@ __global__ void __launch_bounds__(256) fa_append_kv_kernel(uint4* __restrict__ k
                                                            const int32_t* __restrict__ lens,
                                                            int batch, int capacity, int n_new,
                                                            int vecs_per_row, uint32_t* err) {
+    // the attention grid behind this one may start its set-up now; it waits for this
+    // grid's completion before reading the cache
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const long long rows = (long long)batch * n_new;

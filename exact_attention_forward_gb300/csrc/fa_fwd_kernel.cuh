@@ -325,6 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             tma_prefetch_desc(&tm_o);
+            // launched as a programmatic dependent of the cache append (key/value cache
+            // calls): its writes are complete and visible before any load below; a no-op
+            // for other launches
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             const uint64_t pol_q = l2_policy_evict_first();
             const uint64_t pol_kv = l2_policy_evict_last();
             uint32_t ring = 0, ph_qe = 0;  // bit t: parity of the last Q_EMPTY wait of tile t
@@ -925,7 +929,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool FP8>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                       const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t stream) {
+                       const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t stream,
+                       bool after_append) {
     using C = Cfg<D, FP8>;
     static bool attr_done = false;  // per process; the attribute is per function
     if (!attr_done) {
@@ -935,8 +940,24 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    fa_fwd_kernel<D, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, o, p);
-    return cudaGetLastError();
+    if (!after_append) {
+        fa_fwd_kernel<D, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, o, p);
+        return cudaGetLastError();
+    }
+    // after the cache append: programmatic dependent launch, so this grid's set-up
+    // (barriers, TMEM, descriptor prefetch) overlaps the append; the producer waits for
+    // the append's completion (griddepcontrol.wait) before its first load
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, FP8>, q, k, v, o, p);
 }
 
 }  // namespace fa

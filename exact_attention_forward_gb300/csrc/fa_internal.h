@@ -48,13 +48,17 @@ struct FwdParams {
 enum : uint32_t { kErrTimeout = 1u, kErrBadLength = 2u };
 
 // Kernel instances (one translation unit each).
-// q, k, v: TMA load maps; o: TMA store map of the bf16 output (same 4-D view as q)
+// q, k, v: TMA load maps; o: TMA store map of the bf16 output (same 4-D view as q);
+// after_append: launched right behind the cache-append kernel on the same stream
 cudaError_t launch_fwd_bf16_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t s);
+                                const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t s,
+                                bool after_append);
 cudaError_t launch_fwd_bf16_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                 const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t s);
+                                 const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t s,
+                                bool after_append);
 cudaError_t launch_fwd_e4m3_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                 const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t s);
+                                 const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t s,
+                                bool after_append);
 cudaError_t launch_append_kv(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                              const int32_t* cache_seqlens, int batch, int capacity, int n_new,
                              long long row_bytes, uint32_t* err, cudaStream_t s);
