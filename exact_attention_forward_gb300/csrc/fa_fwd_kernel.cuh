@@ -504,15 +504,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_bar(bar(C::KV_FULL + kslot0), (ring / C::kStages) & 1u, wc, SITE_KV_FULL))
                     break;
                 ++ring;
+                // FP8: a tile's last QK^T is the one for block lo; once it completes, the
+                // producer may load the next item's Q over this one while the last PVs run
+                // (measured: +5 % on FP8, -2 to -4 % on bf16, which releases Q at the item end)
                 if (j0 < hi0) {
                     issue_qk(std::integral_constant<int, 0>{}, kslot0);
                     umma_commit(bar(C::S_FULL + 0));
+                    if (FP8 && j0 == lo) umma_commit(bar(C::Q_EMPTY + 0));
                 } else {
                     mbar_arrive(bar(C::KV_EMPTY + kslot0));  // tile 0 never reads K(j0)
                 }
                 if (j0 < hi1) {
                     issue_qk(std::integral_constant<int, 1>{}, kslot0);
                     umma_commit(bar(C::S_FULL + 1));
+                    if (FP8 && j0 == lo) umma_commit(bar(C::Q_EMPTY + 1));
                 } else {
                     mbar_arrive(bar(C::KV_EMPTY + kslot0));
                 }
@@ -554,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             issue_qk(tc, nslot);
                             umma_commit(bar(C::S_FULL + t));
+                            if (FP8 && j - 1 == lo) umma_commit(bar(C::Q_EMPTY + t));
                         } else if (cur) {
                             umma_commit(bar(C::O_FULL + t));  // last block of tile t
                         }
@@ -570,8 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (aborted) break;
-                if (has0) umma_commit(bar(C::Q_EMPTY + 0));
-                if (has1) umma_commit(bar(C::Q_EMPTY + 1));
+                if (!FP8 && has0) umma_commit(bar(C::Q_EMPTY + 0));
+                if (!FP8 && has1) umma_commit(bar(C::Q_EMPTY + 1));
                 ph_q ^= (has0 ? 1u : 0u) | (has1 ? 2u : 0u);
                 ph_o ^= (has0 ? 1u : 0u) | (has1 ? 2u : 0u);
             }
