@@ -74,13 +74,20 @@ def _bytes(w, x) -> float:
 
 
 def _source_sha() -> str:
-    """Hash of the kernel sources, to tell whether recorded ncu counters still apply."""
+    """Hash of the kernel sources with comments and blank lines removed (the sources hold
+    no comment markers inside strings), to tell whether recorded ncu counters still apply:
+    a change of code changes it, a change of comments does not."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_forward_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(f.encode() + code.encode())
     return h.hexdigest()[:16]
 
 
