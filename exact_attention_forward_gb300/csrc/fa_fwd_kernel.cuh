@@ -400,23 +400,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const int kv_head = it.h / p.kv_group;  // grouped-query: shared K/V head
-                for (int j = has_work ? it.n_hi - 1 : it.n_lo - 1; j >= it.n_lo && !aborted; --j) {
-                    const int krow = (p.varlen ? it.k_row0 : 0) + j * kBN;
+                // K/V go through the ring in the order K(n_hi-1), V(n_hi-1), K(n_hi-2), ...,
+                // V(n_lo), one slot each, and are signalled in groups: {K(n_hi-1)},
+                // {V(j), K(j-1)} for each later block, {V(n_lo)} -- the MMA issuer needs V(j)
+                // and K(j-1) at the same point, so one wait covers both.  A group completes
+                // the KV_FULL barrier of its first slot.
+                auto free_slot = [&](uint32_t pos) -> bool {
+                    return wait_bar(bar(C::KV_EMPTY + pos % C::kStages),
+                                    ((pos / C::kStages) & 1u) ^ 1u, wc, SITE_KV_EMPTY);
+                };
+                auto load_kv = [&](uint32_t pos, bool is_v, int j, uint32_t full) {
 #pragma unroll
-                    for (int kv = 0; kv < 2; ++kv) {
-                        const uint32_t slot = ring % C::kStages;
-                        const uint32_t ph = (ring / C::kStages) & 1u;
-                        if (!wait_bar(bar(C::KV_EMPTY + slot), ph ^ 1u, wc, SITE_KV_EMPTY)) {
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_4d(s_kv + (pos % C::kStages) * C::kTileBytes + c * C::kChunkBytes,
+                                    is_v ? &tm_v : &tm_k, full, c * C::kChunkElems, kv_head,
+                                    (p.varlen ? it.k_row0 : 0) + j * kBN, bc, pol_kv);
+                };
+                if (has_work) {
+                    const int j0 = it.n_hi - 1;
+                    if (!free_slot(ring)) {
+                        aborted = true;
+                        break;
+                    }
+                    uint32_t full = bar(C::KV_FULL + ring % C::kStages);
+                    mbar_arrive_expect_tx(full, C::kTileBytes);
+                    load_kv(ring, false, j0, full);
+                    ++ring;
+                    for (int j = j0; j >= it.n_lo; --j) {
+                        const bool pair = j > it.n_lo;  // V(j) with K(j-1), or V(n_lo) alone
+                        if (!free_slot(ring) || (pair && !free_slot(ring + 1))) {
                             aborted = true;
                             break;
                         }
-                        mbar_arrive_expect_tx(bar(C::KV_FULL + slot), C::kTileBytes);
-#pragma unroll
-                        for (int c = 0; c < C::kChunks; ++c)
-                            tma_load_4d(s_kv + slot * C::kTileBytes + c * C::kChunkBytes,
-                                        kv ? &tm_v : &tm_k, bar(C::KV_FULL + slot),
-                                        c * C::kChunkElems, kv_head, krow, bc, pol_kv);
-                        ++ring;
+                        full = bar(C::KV_FULL + ring % C::kStages);
+                        mbar_arrive_expect_tx(full, (pair ? 2u : 1u) * C::kTileBytes);
+                        load_kv(ring, true, j, full);
+                        if (pair) load_kv(ring + 1, false, j - 1, full);
+                        ring += pair ? 2u : 1u;
                     }
                 }
                 if (aborted) break;
@@ -455,6 +475,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto desc = [&](uint32_t lo) -> uint64_t { return ((uint64_t)d_hi << 32) | lo; };
             uint32_t ring = 0;
             uint32_t ph_q = 0, ph_p = 0, ph_o = 0;  // bit t: parity of the next wait on tile t
+            uint32_t ph_kv = 0;  // bit s: parity of the next wait on KV_FULL[s] (armed per group)
+            auto wait_kv = [&](uint32_t slot) -> bool {
+                if (!wait_bar(bar(C::KV_FULL + slot), (ph_kv >> slot) & 1u, wc, SITE_KV_FULL)) return false;
+                ph_kv ^= 1u << slot;
+                return true;
+            };
             bool aborted = false;
             // S_t = Q_t K^T : A = Q (K-major), B = K (K-major), both 128B-swizzled.
             auto issue_qk = [&](auto tc, uint32_t kslot) {
@@ -508,8 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t acc0 = 0u, acc1 = 0u;  // becomes 1 after the tile's first PV
                 const int j0 = it.n_hi - 1;
                 const uint32_t kslot0 = ring % C::kStages;
-                if (!wait_bar(bar(C::KV_FULL + kslot0), (ring / C::kStages) & 1u, wc, SITE_KV_FULL))
-                    break;
+                if (!wait_kv(kslot0)) break;  // group {K(j0)}
                 ++ring;
                 // FP8: a tile's last QK^T is the one for block lo; once it completes, the
                 // producer may load the next item's Q over this one while the last PVs run
@@ -530,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 for (int j = j0; j >= lo; --j) {
                     const uint32_t vslot = ring % C::kStages;
-                    if (!wait_bar(bar(C::KV_FULL + vslot), (ring / C::kStages) & 1u, wc, SITE_KV_FULL)) {
+                    if (!wait_kv(vslot)) {  // group {V(j), K(j-1)} (or {V(lo)})
                         aborted = true;
                         break;
                     }
@@ -540,10 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (j >= hi0) mbar_arrive(bar(C::KV_EMPTY + vslot));
                     if (j >= hi1) mbar_arrive(bar(C::KV_EMPTY + vslot));
                     const bool has_next = j - 1 >= lo;
-                    const uint32_t nslot = ring % C::kStages;
-                    const uint32_t nph = (ring / C::kStages) & 1u;
+                    const uint32_t nslot = ring % C::kStages;  // K(j-1), landed with V(j)
                     if (has_next) ++ring;
-                    bool next_ready = false;
                     // one tile: PV_t(j) if it visits block j, then S_t(j-1) if it visits j-1
                     auto tile_step = [&](auto tc, int hi, uint32_t& acc) -> bool {
                         constexpr int t = decltype(tc)::value;
@@ -560,10 +583,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             acc = 1u;
                         }
                         if (nxt) {
-                            if (!next_ready) {
-                                if (!wait_bar(bar(C::KV_FULL + nslot), nph, wc, SITE_KV_FULL)) return false;
-                                next_ready = true;
-                            }
                             issue_qk(tc, nslot);
                             umma_commit(bar(C::S_FULL + t));
                             if (FP8 && j - 1 == lo) umma_commit(bar(C::Q_EMPTY + t));
