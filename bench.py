@@ -10,7 +10,8 @@ workload (default: bf16, causal, B=2 H=32 S=8192 D=128, inputs 2*N(0,1)):
 and the L2 flushed between timed steps (a 256 MiB write, then a 256 MiB read so no
 dirty lines are left to write back during the timed step); `e2e` is the same
 metric through the public API with pinned host inputs copied in and O/LSE
-copied out inside the timed region.  Under torchrun each rank runs the same
+copied out inside the timed region (steps pipelined over copy-in, compute and
+copy-out streams with two buffer sets, as a serving loop runs them).  Under torchrun each rank runs the same
 workload on its own GPU (the pass shards over independent (batch, head)
 problems; no collective on the data path): value = all ranks' FLOPs / the
 slowest rank's time.
@@ -406,48 +407,70 @@ def run_gpu(args, w):
     # ---------------- end to end through the public API, host buffers
     e2e = None
     if not args.skip_e2e:
-        # per step, the inputs come from pinned host memory: Q, K, V -- or, for a cache
-        # workload, Q, the new K/V rows and the cache lengths (the cache itself is state
-        # that lives on the device)
+        # Per step, the inputs come from pinned host memory -- Q, K, V, or for a cache
+        # workload Q, the new K/V rows and the cache lengths (the cache itself is state that
+        # lives on the device) -- and O and LSE go back to pinned host memory.  Steps are
+        # pipelined the way a serving loop would run them: copies in on one stream, the
+        # forward pass on another, copies out on a third, two buffer sets in rotation, so
+        # step i+1's inputs travel while step i computes.
         names = ("q", "k_new", "v_new", "cache_seqlens") if cache is not None else ("q", "k", "v")
+        nbuf = 2
         host = {n: x[n].cpu().contiguous().pin_memory() for n in names}
-        devb = {n: torch.empty_like(host[n], device=dev) for n in names}
-        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        devb = [{n: torch.empty_like(host[n], device=dev) for n in names} for _ in range(nbuf)]
+        outs = [(torch.empty_like(o), torch.empty_like(lse)) for _ in range(nbuf)]
+        hres = [(torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                 torch.empty(lse.shape, dtype=lse.dtype).pin_memory()) for _ in range(nbuf)]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+        ev_comp = [torch.cuda.Event() for _ in range(nbuf)]
+        ev_out = [torch.cuda.Event() for _ in range(nbuf)]
 
-        def e2e_step():
-            for n in names:
-                devb[n].copy_(host[n], non_blocking=True)
+        def e2e_step(i):
+            bi = i % nbuf
+            d, (oo, ll), (ho, hl) = devb[bi], outs[bi], hres[bi]
+            with torch.cuda.stream(s_in):
+                if i >= nbuf:
+                    s_in.wait_event(ev_comp[bi])  # step i-nbuf's pass has read these inputs
+                for n in names:
+                    d[n].copy_(host[n], non_blocking=True)
+                ev_in[bi].record(s_in)
+            stream.wait_event(ev_in[bi])
+            if i >= nbuf:
+                stream.wait_event(ev_out[bi])  # step i-nbuf's results have left these buffers
             if cache is not None:
-                oo, ll = fa.fwd_kvcache(devb["q"], k, v, devb["cache_seqlens"], devb["k_new"],
-                                        devb["v_new"], causal=w.causal,
-                                        softmax_scale=w.softmax_scale, descale=descale,
-                                        workspace=ws, out=o, lse=lse, stream=stream)
+                fa.fwd_kvcache(d["q"], k, v, d["cache_seqlens"], d["k_new"], d["v_new"],
+                               causal=w.causal, softmax_scale=w.softmax_scale, descale=descale,
+                               workspace=ws, out=oo, lse=ll, stream=stream)
             else:
-                oo, ll = fa.fwd(devb["q"], devb["k"], devb["v"], causal=w.causal,
-                                softmax_scale=w.softmax_scale, cu_seqlens_q=cu_q,
-                                cu_seqlens_k=cu_k, max_seqlen_q=x["max_seqlen_q"],
-                                max_seqlen_k=x["max_seqlen_k"], descale=descale, workspace=ws,
-                                out=o, lse=lse, stream=stream)
-            ho.copy_(oo, non_blocking=True)
-            hl.copy_(ll, non_blocking=True)
+                fa.fwd(d["q"], d["k"], d["v"], causal=w.causal, softmax_scale=w.softmax_scale,
+                       cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=x["max_seqlen_q"],
+                       max_seqlen_k=x["max_seqlen_k"], descale=descale, workspace=ws, out=oo,
+                       lse=ll, stream=stream)
+            ev_comp[bi].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[bi])
+                ho.copy_(oo, non_blocking=True)
+                hl.copy_(ll, non_blocking=True)
+                ev_out[bi].record(s_out)
 
-        for _ in range(2):
-            e2e_step()
+        for i in range(2 * nbuf):
+            e2e_step(i)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         n_e2e = max(3, min(args.steps, 20))
         if world > 1:
             dist.barrier()
-        e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
+        e0.record(s_in)
+        for i in range(n_e2e):
+            e2e_step(i)
+        s_out.wait_stream(stream)
+        s_out.wait_stream(s_in)
+        e1.record(s_out)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
         h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        d2h = sum(t.numel() * t.element_size() for t in hres[0])
         e2e = {"value": job_throughput(flops, world, n_e2e, e2e_ms) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms / n_e2e}
