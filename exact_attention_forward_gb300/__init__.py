@@ -42,7 +42,7 @@ FA_DTYPE_BF16, FA_DTYPE_E4M3, FA_DTYPE_E5M2 = 0, 1, 2
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_num_splits", "fa_status_string",
                     "fa_last_error_detail", "fa_device_error", "fa_debug_set",
                     "fa_fwd_static_workspace", "fa_fwd_gqa", "fa_fwd_fp8", "fa_fwd_kvcache",
-                    "fa_fwd_workspace_size_gqa", "fa_fwd_num_splits_gqa")
+                    "fa_fwd_workspace_size_gqa", "fa_fwd_num_splits_gqa", "fa_fwd_2cta")
 
 _lock = threading.Lock()
 _lib = None
@@ -101,6 +101,9 @@ def load_library():
         lib.fa_fwd_kvcache.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp,
                                        i32, i32, f32, i32, i32, i32, vp, vp, vp, i64, i64, vp, sz,
                                        vp]
+        lib.fa_fwd_2cta.restype = i32
+        lib.fa_fwd_2cta.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, i32,
+                                    i32, f32, i32, vp]
         lib.fa_fwd_static_workspace.restype = i32
         lib.fa_fwd_static_workspace.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                                 f32, i32, i32, vp, vp, vp, vp]
@@ -179,7 +182,7 @@ def _fp8_descales(descale, batch, heads_k, dev, temps):
 
 def fwd(q, k, v, *, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seqlens_k=None,
         max_seqlen_q=None, max_seqlen_k=None, descale=None, workspace="auto", out=None,
-        lse=None, stream=None):
+        lse=None, stream=None, cta_pair=False):
     """Attention forward on the current CUDA device.  Returns (o, lse).
 
     descale: for FP8 inputs, (q, k, v) descales as python floats, 0-d fp32 CUDA
@@ -188,6 +191,8 @@ def fwd(q, k, v, *, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
     workspace: "auto" (allocated with torch when the shape benefits from
     splitting the key range), None (never split) or a caller-owned uint8 CUDA
     tensor.
+    cta_pair: run the CTA-pair kernel (fa_fwd_2cta: bf16, head dim 128, no key
+    splits; the workspace argument is then unused).
     """
     import torch
 
@@ -241,6 +246,8 @@ def fwd(q, k, v, *, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
         ds, ds_b, ds_h = _fp8_descales(descale, batch, heads_k, dev, temps)
     ws = None
     ws_bytes = 0
+    if cta_pair:
+        workspace = None
     if isinstance(workspace, str):
         if workspace != "auto":
             raise ValueError('workspace must be "auto", None or a uint8 CUDA tensor')
@@ -255,7 +262,15 @@ def fwd(q, k, v, *, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
         ws_bytes = workspace.numel() * workspace.element_size()
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    if dt == FA_DTYPE_E4M3 and (v_e5m2 or ds_b or ds_h):
+    if cta_pair:
+        if dt != FA_DTYPE_BF16 or d != dv:
+            raise ValueError("cta_pair needs bf16 inputs with head_dim == head_dim_v")
+        st = lib.fa_fwd_2cta(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(batch),
+                             int(heads), int(heads_k), int(sq_arg), int(sk_arg),
+                             _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), mq, mk, int(d),
+                             float(softmax_scale), int(bool(causal)),
+                             ctypes.c_void_p(stream.cuda_stream))
+    elif dt == FA_DTYPE_E4M3 and (v_e5m2 or ds_b or ds_h):
         if d != dv:
             raise ValueError("FP8 needs head_dim == head_dim_v")
         st = lib.fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(batch),

@@ -20,7 +20,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "_fa_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["fa_api.cu", "fa_fwd_bf16_d64.cu", "fa_fwd_bf16_d128.cu", "fa_fwd_e4m3_d128.cu",
-           "fa_static_ws.cu", "fa_append_kv.cu"]
+           "fa_fwd_pair_bf16_d128.cu", "fa_static_ws.cu", "fa_append_kv.cu"]
 
 
 def _nvcc():

@@ -89,15 +89,16 @@ uint32_t* next_sched_slot(int dev) {
 // 4-D view (d, head, row, batch) of a [batch, rows, heads, d] tensor; box =
 // one 128-byte swizzle atom of d by 128 rows of one head, or (box_heads > 1) by
 // box_heads heads x 128 / box_heads rows -- 128 shared-memory rows either way.
+// box_rows > 0 overrides the rows of a box (a CTA pair loads 64-key halves of K blocks).
 fa_status encode_map(CUtensorMap* m, const void* base, bool fp8, int d, int heads, int rows,
-                     int batch, int box_heads = 1) {
+                     int batch, int box_heads = 1, int box_rows = 0) {
     const int elem = fp8 ? 1 : 2;
     cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1),
                           (cuuint64_t)(batch > 0 ? batch : 1)};
     cuuint64_t strides[3] = {(cuuint64_t)d * elem, (cuuint64_t)heads * d * elem,
                              (cuuint64_t)(rows > 0 ? rows : 1) * heads * d * elem};
     cuuint32_t box[4] = {(cuuint32_t)(128 / elem), (cuuint32_t)box_heads,
-                         (cuuint32_t)(128 / box_heads), 1u};
+                         (cuuint32_t)(box_rows > 0 ? box_rows : 128 / box_heads), 1u};
     cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     CUresult r = g_encode(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                           const_cast<void*>(base), dims, strides, box, estr,
@@ -108,6 +109,21 @@ fa_status encode_map(CUtensorMap* m, const void* base, bool fp8, int d, int head
 }
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// CTA pairs of the pair kernel that fit on the device at once (cached per device).
+int g_pairs[kMaxDevices] = {0};
+fa_status resident_pairs(int dev, int* pairs) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_pairs[dev] == 0) {
+        int n = 0;
+        cudaError_t e = max_resident_pairs_bf16_d128(&n);
+        if (e != cudaSuccess) return fail(FA_ERR_CUDA, "cluster occupancy: %s", cudaGetErrorString(e));
+        if (n < 1) return fail(FA_ERR_UNSUPPORTED, "no CTA pair of the kernel fits on this device");
+        g_pairs[dev] = n;
+    }
+    *pairs = g_pairs[dev];
+    return FA_OK;
+}
 
 // Key splits for a fixed-length shape: only when the (batch, head, tile-pair)
 // items cannot fill the GPU and the key range is long.
@@ -285,6 +301,7 @@ struct FwdArgs {
     void* workspace;
     size_t workspace_bytes;
     void* stream;
+    bool cta_pair;              // run the CTA-pair (cta_group::2) kernel
 };
 
 fa_status fwd_impl(const FwdArgs& a) {
@@ -329,6 +346,9 @@ fa_status fwd_impl(const FwdArgs& a) {
         return fail(FA_ERR_UNSUPPORTED, "bf16 head_dim %d not built (64, 128)", a.head_dim);
     if (fp8 && a.head_dim != 128)
         return fail(FA_ERR_UNSUPPORTED, "fp8 head_dim %d not built (128)", a.head_dim);
+    if (a.cta_pair && (fp8 || a.head_dim != 128 || a.seqused_k || a.n_new > 0 || a.workspace))
+        return fail(FA_ERR_UNSUPPORTED, "the CTA-pair kernel is built for bf16, head_dim 128, "
+                                        "without caches or key splits");
     const long long rows_q = varlen ? a.seqlen_q : (long long)a.batch * a.seqlen_q;
     const long long rows_k = varlen ? a.seqlen_k : (long long)a.batch * a.seqlen_k;
     if (rows_q * a.heads * a.head_dim >= (1ll << 40) ||
@@ -347,7 +367,7 @@ fa_status fwd_impl(const FwdArgs& a) {
     if (st != FA_OK) return st;
 
     // ---------------------------------------------------------------- decomposition
-    const int pack = choose_pack(a.heads, a.heads_k, mq, varlen);
+    const int pack = a.cta_pair ? 1 : choose_pack(a.heads, a.heads_k, mq, varlen);
     int splits = 1;
     if (!varlen && a.workspace && mq > 0) {
         splits = plan_splits(a.batch, a.heads, a.heads_k, a.seqlen_q, a.seqlen_k, a.causal, sms);
@@ -380,7 +400,7 @@ fa_status fwd_impl(const FwdArgs& a) {
     p.seqlen_q = mq;
     p.seqlen_k = mk;
     p.total_q = varlen ? a.seqlen_q : 0;
-    p.n_mpairs = ceil_div((long long)mq * pack, 256);
+    p.n_mpairs = ceil_div((long long)mq * pack, a.cta_pair ? 512 : 256);
     p.n_splits = splits;
     const int nblk = ceil_div(mk > 0 ? mk : 1, 128);
     p.blocks_per_split = splits > 1 ? ceil_div(nblk, splits) : (1 << 29);
@@ -390,7 +410,7 @@ fa_status fwd_impl(const FwdArgs& a) {
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.causal = a.causal;
     p.varlen = varlen ? 1 : 0;
-    p.greedy = varlen ? 1 : 0;  // varlen item costs are unknown on the host
+    p.greedy = varlen && !a.cta_pair ? 1 : 0;  // varlen item costs are unknown on the host
     p.split = splits > 1 ? 1 : 0;
     p.v_e5m2 = a.v_dtype == FA_DTYPE_E5M2 ? 1 : 0;
     if (p.split) {
@@ -416,7 +436,8 @@ fa_status fwd_impl(const FwdArgs& a) {
         tk = tq;
         tv = tq;
     } else {
-        if ((st = encode_map(&tk, a.k, fp8, a.head_dim, a.heads_k, a.seqlen_k, nbat)) != FA_OK)
+        if ((st = encode_map(&tk, a.k, fp8, a.head_dim, a.heads_k, a.seqlen_k, nbat, 1,
+                             a.cta_pair ? 64 : 0)) != FA_OK)
             return st;
         if ((st = encode_map(&tv, a.v, fp8, a.head_dim, a.heads_k, a.seqlen_k, nbat)) != FA_OK)
             return st;
@@ -437,6 +458,14 @@ fa_status fwd_impl(const FwdArgs& a) {
         if (e != cudaSuccess) return fail(FA_ERR_CUDA, "append launch: %s", cudaGetErrorString(e));
     }
     if (rows_q == 0 || mq == 0) return FA_OK;
+    if (a.cta_pair) {
+        int pairs = 0;
+        if ((st = resident_pairs(dev, &pairs)) != FA_OK) return st;
+        const int grid2 = 2 * (int)(n_items < pairs ? n_items : pairs);
+        e = launch_fwd_pair_bf16_d128(tq, tk, tv, to, p, grid2, s);
+        if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
+        return FA_OK;
+    }
     const int grid = (int)(n_items < sms ? n_items : sms);
     if (fp8)
         e = launch_fwd_e4m3_d128(tq, tk, tv, to, p, grid, s, append);
@@ -563,6 +592,26 @@ fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float
     a.qd = q_descale; a.kd = k_descale; a.vd = v_descale;
     a.workspace = workspace; a.workspace_bytes = workspace_bytes;
     a.stream = stream;
+    return fwd_impl(a);
+}
+
+fa_status fa_fwd_2cta(const void* q, const void* k, const void* v, void* o, float* lse, int batch,
+                      int heads, int heads_k, int seqlen_q, int seqlen_k,
+                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int max_seqlen_q,
+                      int max_seqlen_k, int head_dim, float softmax_scale, int causal,
+                      void* stream) {
+    t_detail[0] = '\0';
+    FwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+    a.batch = batch; a.heads = heads; a.heads_k = heads_k;
+    a.seqlen_q = seqlen_q; a.seqlen_k = seqlen_k;
+    a.cu_q = cu_seqlens_q; a.cu_k = cu_seqlens_k;
+    a.max_q = max_seqlen_q; a.max_k = max_seqlen_k;
+    a.head_dim = head_dim; a.head_dim_v = head_dim;
+    a.scale = softmax_scale; a.causal = causal;
+    a.dtype = FA_DTYPE_BF16; a.v_dtype = FA_DTYPE_BF16;
+    a.stream = stream;
+    a.cta_pair = true;
     return fwd_impl(a);
 }
 

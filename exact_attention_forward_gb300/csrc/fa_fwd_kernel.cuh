@@ -58,7 +58,16 @@
 //     and writes it out with a TMA store (plain stores only where a varlen tile
 //     crosses its sequence end, and for the fp32 split partials);
 //   * every wait is bounded by wall clock; a timeout sets the device error
-//     word and all roles abandon the launch cleanly (TMEM released).
+//     word and all roles abandon the launch cleanly (TMEM released);
+//   * CTA-pair variant (PAIR, bf16, D = 128): a cluster of two CTAs on two SMs
+//     runs M = 256 tcgen05 MMAs (cta_group::2) issued by one thread of the even
+//     CTA; a work item is 512 query rows, each of the pair's two MMA row slots
+//     covering 256 rows (128 in each CTA).  Each CTA loads its own halves of the
+//     operands -- its Q rows, keys [64r, 64r+64) of every K block and head-dim
+//     columns [64r, 64r+64) of every V block -- so each SM streams half of each
+//     K/V block through shared memory; the loads complete on the even CTA's
+//     barriers, MMA completions are multicast to both CTAs, and the odd CTA's
+//     softmax warps hand P back to the even CTA's barrier.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -104,8 +113,9 @@ constexpr uint32_t kRegsLoadMma = 104;
 constexpr uint32_t kRegsSoftmax = 200;
 static_assert(128 * kRegsLoadMma + 256 * kRegsSoftmax <= 384 * 168, "register split exceeds launch");
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool PAIR = false>
 struct Cfg {
+    static_assert(!PAIR || (!FP8 && D == 128), "the CTA-pair variant is built for bf16, D = 128");
     static constexpr int kElem = FP8 ? 1 : 2;
     static constexpr int kRowBytes = D * kElem;
     static constexpr int kChunks = kRowBytes / 128;        // 128-byte swizzle atoms per row
@@ -113,14 +123,18 @@ struct Cfg {
     static constexpr int kChunkBytes = kBM * 128;          // one atom column of a tile: 16 KiB
     static constexpr int kTileBytes = kBM * kRowBytes;     // Q tile == K/V block (BM == BN)
     static constexpr int kUmmaK = 32 / kElem;              // reduction depth of one MMA
-    static constexpr int kStages = (FP8 || D == 64) ? 8 : 4;
+    // a K/V ring slot holds one K or V block, or (CTA pair) this CTA's half of one:
+    // 64 keys of K, or 64 head-dim columns of V
+    static constexpr int kSlotBytes = PAIR ? kTileBytes / 2 : kTileBytes;
+    static constexpr int kKChunkBytes = PAIR ? kBN / 2 * 128 : kChunkBytes;  // atom column of a K slot
+    static constexpr int kStages = (FP8 || D == 64 || PAIR) ? 8 : 4;
     static constexpr int kPCols = kBN * kElem / 4;         // TMEM columns of a P tile
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = kTiles * kTileBytes;
     // epilogue staging: per tile, 128 rows x 64 bf16 columns of O (one 128-byte swizzle atom
     // wide), stored to HBM by TMA; a D = 128 tile goes out in two halves
     static constexpr int kStageBytes = kBM * 128;
-    static constexpr int kStageOff = kKVOff + kStages * kTileBytes;
+    static constexpr int kStageOff = kKVOff + kStages * kSlotBytes;
     static constexpr int kBarOff = kStageOff + kTiles * kStageBytes;
     enum {
         Q_FULL = 0, Q_EMPTY = 2, S_FULL = 4, P_FULL = 6, O_FULL = 8, O_EMPTY = 10, STG_FULL = 12,
@@ -129,8 +143,9 @@ struct Cfg {
     };
     static constexpr int kMiscOff = kBarOff + NUM_BARS * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1 KiB
-    static constexpr uint32_t kIdescQK = make_idesc(kBM, kBN, 0u + (FP8 ? 0u : 1u), false);
-    static constexpr uint32_t kIdescPV = make_idesc(kBM, D, 0u + (FP8 ? 0u : 1u), true);
+    static constexpr int kMmaM = PAIR ? 2 * kBM : kBM;  // rows of one MMA (both CTAs of a pair)
+    static constexpr uint32_t kIdescQK = make_idesc(kMmaM, kBN, 0u + (FP8 ? 0u : 1u), false);
+    static constexpr uint32_t kIdescPV = make_idesc(kMmaM, D, 0u + (FP8 ? 0u : 1u), true);
     // FP8 with an E5M2 V: P (A operand) stays E4M3, B = V is E5M2 (kind::f8f6f4 codes 0 / 1)
     static constexpr uint32_t kIdescPV5 = make_idesc2(kBM, D, 0u, 1u, true);
     static constexpr uint32_t kColO = 256;
@@ -140,7 +155,9 @@ struct Cfg {
 };
 
 // One unit of work: a pair of 128-row query tiles of one (batch, head) and a
-// range of key blocks.  Decoded identically by every role from its index.
+// range of key blocks.  Decoded identically by every role from its index.  In a CTA
+// pair an item is two 256-row MMA slots; m0 is then this CTA's half of slot t, and the
+// key ranges and `active` belong to the slot (both CTAs visit the same blocks).
 struct Item {
     int b, h, split;
     int sq, sk;          // this sequence's lengths
@@ -156,7 +173,9 @@ struct Item {
 // causal mask later pairs see more key blocks), then (batch, head, split).  Query
 // heads sharing a K/V head (grouped-query attention) are consecutive items, so
 // they stream the same K/V at about the same time and share it in L2.
-__device__ __forceinline__ Item decode_item(const FwdParams& p, int w) {
+template <bool PAIR>
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int w, uint32_t rank) {
+    constexpr int kSlotRows = PAIR ? 2 * kBM : kBM;  // query rows of one MMA row slot
     Item it;
     // packed grouped-query mode (p.pack = G > 1): an item serves one K/V head, and its
     // tile rows are (query row, query head of the group) pairs, row-major: packed row
@@ -192,11 +211,12 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int w) {
     it.n_hi = it.n_lo;
 #pragma unroll
     for (int t = 0; t < kTiles; ++t) {
-        it.m0[t] = mp * (kTiles * kBM) + t * kBM;  // first (packed) row of the tile
-        it.active[t] = it.m0[t] < it.sq * G;
+        const int s0 = mp * (kTiles * kSlotRows) + t * kSlotRows;  // first (packed) row of slot t
+        it.m0[t] = s0 + (PAIR ? (int)rank * kBM : 0);               // ... of this CTA's tile
+        it.active[t] = s0 < it.sq * G;
         int hi = n_end;
         if (p.causal) {
-            const int rmax = (min(it.m0[t] + kBM, it.sq * G) - 1) / G;  // last query row
+            const int rmax = (min(s0 + kSlotRows, it.sq * G) - 1) / G;  // last query row
             const int last = rmax + it.sk - it.sq;  // last visible key of the tile's last row
             hi = last < 0 ? 0 : min(hi, last / kBN + 1);
         }
@@ -218,9 +238,10 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int w) {
 //    comes from a device-wide counter (atomicAdd), so a CTA that finishes early takes
 //    the next (in LPT order: the next most expensive) item.
 constexpr uint32_t kItemConsumers = 1 + 2 * (kBM / 32);  // issuer + one arrival per softmax warp
-__device__ __forceinline__ int item_of_round(int round, int nctas) {
-    const int pos = (round & 1) ? (nctas - 1 - (int)blockIdx.x) : (int)blockIdx.x;
-    return round * nctas + pos;
+// `unit`: this CTA (or CTA pair) among `nunits`
+__device__ __forceinline__ int item_of_round(int round, int unit, int nunits) {
+    const int pos = (round & 1) ? (nunits - 1 - unit) : unit;
+    return round * nunits + pos;
 }
 
 struct WaitCtx {
@@ -229,13 +250,15 @@ struct WaitCtx {
     volatile uint32_t* abort_flag;  // shared memory
 };
 
+// cluster: acquire at cluster scope (barriers that the peer CTA of a pair arrives on)
 static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w,
-                                                 uint32_t site, bool honor_abort = true) {
+                                                 uint32_t site, bool honor_abort = true,
+                                                 bool cluster = false) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 128; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (honor_abort && *w.abort_flag) return false;
         if (globaltimer_ns() - t0 > w.limit_ns) {
             atomicCAS(w.err, 0u, kErrTimeout | (site << 8));
@@ -251,6 +274,11 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
     if (mbar_try_wait(bar, parity)) return true;
     return wait_slow(bar, parity, w, site);
 }
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                                 uint32_t site) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    return wait_slow(bar, parity, w, site, true, true);
+}
 
 // Wait-site codes reported in bits 8..15 of the error word.
 enum : uint32_t {
@@ -259,12 +287,12 @@ enum : uint32_t {
     SITE_STG_EMPTY = 11, SITE_ITEM_FULL = 12, SITE_ITEM_EMPTY = 13
 };
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdParams p) {
-    using C = Cfg<D, FP8>;
+    using C = Cfg<D, FP8, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -279,15 +307,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // CTA pair: rank 0 issues the MMAs and owns the barriers the pair's loads and P / O
+    // hand-offs complete; `leader(b)` is that barrier's shared::cluster address
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    // (the barrier array is contiguous in each CTA's window, so one mapping serves all)
+    const uint32_t s_bar_lead = PAIR ? mapa_shared(s_bar, 0u) : s_bar;
+    auto leader = [&](uint32_t b) -> uint32_t { return PAIR ? s_bar_lead + (b - s_bar) : b; };
+    // the unit the static schedule hands items to: this CTA, or this CTA's pair
+    const int unit = PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
+    const int nunits = PAIR ? (int)ncluster_x() : (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < kTiles; ++t) {
             mbar_init(bar(C::Q_FULL + t), 1);
             mbar_init(bar(C::Q_EMPTY + t), 1);
             mbar_init(bar(C::S_FULL + t), 1);
-            mbar_init(bar(C::P_FULL + t), kBM / 32);   // one arrival per softmax warp
+            // one arrival per softmax warp (of both CTAs of a pair)
+            mbar_init(bar(C::P_FULL + t), (PAIR ? 2 : 1) * kBM / 32);
             mbar_init(bar(C::O_FULL + t), 1);
-            mbar_init(bar(C::O_EMPTY + t), kBM / 32);
+            mbar_init(bar(C::O_EMPTY + t), (PAIR ? 2 : 1) * kBM / 32);
             mbar_init(bar(C::STG_FULL + t), kBM / 32);  // every warp of the tile wrote its rows
             mbar_init(bar(C::STG_EMPTY + t), 1);        // the store has read the staging rows
         }
@@ -305,11 +343,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+            tmem_relinquish();
+        }
         tc_fence_before();
     }
-    __syncthreads();
+    // a pair's barriers are initialised before the other CTA's loads, commits or arrivals
+    // can reach them
+    if constexpr (PAIR) {
+        __syncwarp();  // the .aligned cluster barrier wants converged warps
+        cluster_sync();
+    } else {
+        __syncthreads();
+    }
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtx wc{p.wait_limit_ns, p.err, abort_flag};
@@ -364,15 +414,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p.sched[1] = 0u;
                 }
             };
-            int w_next = (int)blockIdx.x;
+            // a pair's two producers follow one static order (no device counter)
+            const bool greedy = !PAIR && p.greedy;
+            int w_next = unit;
             int round_no = 0;  // static order: rounds of the snake
             if (!publish(w_next)) aborted = true;
             for (int w = w_next; !aborted && w < p.n_items; w = w_next) {
                 // the next index is requested now and published once this item's loads have
                 // been issued, so the counter's round trip overlaps them
                 ++round_no;
-                const uint32_t ticket = p.greedy ? atomicAdd(p.sched, 1u) : 0u;
-                const Item it = decode_item(p, w);
+                const uint32_t ticket = greedy ? atomicAdd(p.sched, 1u) : 0u;
+                const Item it = decode_item<PAIR>(p, w, rank);
                 const int bc = p.varlen ? 0 : it.b;  // batch coordinate of the 4-D view
                 auto load_q = [&](auto tc) -> bool {
                     constexpr int t = decltype(tc)::value;
@@ -386,11 +438,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     // packed mode: the map's box spans G heads x 128/G rows
                     const int qrow = (p.varlen ? it.q_row0 : 0) + it.m0[t] / p.pack;
-                    mbar_arrive_expect_tx(bar(C::Q_FULL + t), C::kTileBytes);
+                    // a pair's Q tiles both land on the even CTA's barrier, which expects them
+                    if (rank == 0u) mbar_arrive_expect_tx(bar(C::Q_FULL + t), (PAIR ? 2 : 1) * C::kTileBytes);
 #pragma unroll
-                    for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_4d(s_q + t * C::kTileBytes + c * C::kChunkBytes, &tm_q,
-                                    bar(C::Q_FULL + t), c * C::kChunkElems, it.h, qrow, bc, pol_q);
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        if constexpr (PAIR)
+                            tma_load_4d_pair(s_q + t * C::kTileBytes + c * C::kChunkBytes, &tm_q,
+                                             leader(bar(C::Q_FULL + t)), c * C::kChunkElems, it.h, qrow,
+                                             bc, pol_q);
+                        else
+                            tma_load_4d(s_q + t * C::kTileBytes + c * C::kChunkBytes, &tm_q,
+                                        bar(C::Q_FULL + t), c * C::kChunkElems, it.h, qrow, bc, pol_q);
+                    }
                     return true;
                 };
                 const bool has_work = it.n_hi > it.n_lo;
@@ -410,11 +469,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     ((pos / C::kStages) & 1u) ^ 1u, wc, SITE_KV_EMPTY);
                 };
                 auto load_kv = [&](uint32_t pos, bool is_v, int j, uint32_t full) {
+                    const uint32_t dst = s_kv + (pos % C::kStages) * C::kSlotBytes;
+                    const int row = (p.varlen ? it.k_row0 : 0) + j * kBN;
+                    if constexpr (PAIR) {
+                        // this CTA's half: head-dim columns [64r, 64r+64) of V(j) (one atom
+                        // column, 128 keys), or keys [64r, 64r+64) of K(j) (64-row boxes)
+                        const uint32_t fl = leader(full);
+                        if (is_v) {
+                            tma_load_4d_pair(dst, &tm_v, fl, (int)rank * C::kChunkElems, kv_head, row, bc,
+                                             pol_kv);
+                        } else {
 #pragma unroll
-                    for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_4d(s_kv + (pos % C::kStages) * C::kTileBytes + c * C::kChunkBytes,
-                                    is_v ? &tm_v : &tm_k, full, c * C::kChunkElems, kv_head,
-                                    (p.varlen ? it.k_row0 : 0) + j * kBN, bc, pol_kv);
+                            for (int c = 0; c < C::kChunks; ++c)
+                                tma_load_4d_pair(dst + c * C::kKChunkBytes, &tm_k, fl, c * C::kChunkElems,
+                                                 kv_head, row + (int)rank * (kBN / 2), bc, pol_kv);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_4d(dst + c * C::kChunkBytes, is_v ? &tm_v : &tm_k, full,
+                                        c * C::kChunkElems, kv_head, row, bc, pol_kv);
+                    }
+                };
+                // bytes a group of n slots brings to its barrier (both CTAs' halves in a pair;
+                // only the even CTA, which owns the barrier, announces them)
+                auto expect_group = [&](uint32_t full, uint32_t n) {
+                    if (rank == 0u) mbar_arrive_expect_tx(full, n * (PAIR ? 2u : 1u) * C::kSlotBytes);
                 };
                 if (has_work) {
                     const int j0 = it.n_hi - 1;
@@ -423,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     uint32_t full = bar(C::KV_FULL + ring % C::kStages);
-                    mbar_arrive_expect_tx(full, C::kTileBytes);
+                    expect_group(full, 1u);
                     load_kv(ring, false, j0, full);
                     ++ring;
                     for (int j = j0; j >= it.n_lo; --j) {
@@ -433,25 +513,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         full = bar(C::KV_FULL + ring % C::kStages);
-                        mbar_arrive_expect_tx(full, (pair ? 2u : 1u) * C::kTileBytes);
+                        expect_group(full, pair ? 2u : 1u);
                         load_kv(ring, true, j, full);
                         if (pair) load_kv(ring + 1, false, j - 1, full);
                         ring += pair ? 2u : 1u;
                     }
                 }
                 if (aborted) break;
-                if (p.greedy) {
+                if (greedy) {
                     w_next = min((int)(gridDim.x + ticket), p.n_items);
                     if (w_next >= p.n_items) fetching_done();
                 } else {
-                    w_next = min(item_of_round(round_no, (int)gridDim.x), p.n_items);
+                    w_next = min(item_of_round(round_no, unit, nunits), p.n_items);
                 }
                 if (!publish(w_next)) {
                     aborted = true;
                     break;
                 }
             }
-            if (p.greedy) fetching_done();  // after an abort, or with no item beyond the first
+            if (greedy) fetching_done();  // after an abort, or with no item beyond the first
             if (aborted) {  // let copies already in flight land before the CTA retires
                 const uint64_t t0 = globaltimer_ns();
                 while (globaltimer_ns() - t0 < 200000ull) {
@@ -465,13 +545,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         // it is kept lean: tiles are unrolled at compile time (phase bits live in
         // registers), and descriptors are built once -- per MMA only the 32-bit low
         // word (start address) advances.
-        if (lane == 0) {
+        if (PAIR && rank != 0u && lane == 0) {
+            // the odd CTA of a pair issues nothing; it only keeps its item ring turning
+            for (;;) {
+                int w;
+                if (!read_item(w)) break;
+                mbar_arrive(bar(C::ITEM_EMPTY + ((items_read - 1) & 1u)));
+                if (w >= p.n_items) break;
+            }
+        } else if (lane == 0) {
             // descriptor words: high word (SBO = 1024 B, version 1, 128B swizzle) is common
             const uint32_t d_hi = (uint32_t)(sdesc_sw128(0, 16, 1024) >> 32);
             const uint32_t q_lo = (uint32_t)sdesc_sw128(s_q, 16, 1024);          // + t*tile
-            const uint32_t k_lo = (uint32_t)sdesc_sw128(s_kv, 16, 1024);         // + slot*tile
+            const uint32_t k_lo = (uint32_t)sdesc_sw128(s_kv, 16, 1024);         // + slot*slot bytes
             const uint32_t v_lo = (uint32_t)sdesc_sw128(s_kv, C::kChunkBytes, 1024);
             constexpr uint32_t kTile16 = C::kTileBytes >> 4;
+            constexpr uint32_t kSlot16 = C::kSlotBytes >> 4;
+            // MMA completions reach both CTAs of a pair
+            auto commit = [&](uint32_t b) {
+                if constexpr (PAIR)
+                    umma_commit_pair_mc(b, (uint16_t)0x3);
+                else
+                    umma_commit(b);
+            };
+            // a K/V slot that a tile does not read is released for it (in both CTAs of a pair)
+            const uint32_t kv_empty_peer = PAIR ? mapa_shared(bar(C::KV_EMPTY), 1u) : 0u;
+            auto release_slot = [&](uint32_t slot) {
+                mbar_arrive(bar(C::KV_EMPTY + slot));
+                if constexpr (PAIR) mbar_arrive_cluster(kv_empty_peer + 8u * slot);
+            };
+            // P and O hand-offs: a pair's odd CTA arrives from the other SM
+            auto wait_handoff = [&](uint32_t b, uint32_t parity, uint32_t site) -> bool {
+                return PAIR ? wait_bar_cluster(b, parity, wc, site) : wait_bar(b, parity, wc, site);
+            };
             auto desc = [&](uint32_t lo) -> uint64_t { return ((uint64_t)d_hi << 32) | lo; };
             uint32_t ring = 0;
             uint32_t ph_q = 0, ph_p = 0, ph_o = 0;  // bit t: parity of the next wait on tile t
@@ -485,17 +591,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             // S_t = Q_t K^T : A = Q (K-major), B = K (K-major), both 128B-swizzled.
             auto issue_qk = [&](auto tc, uint32_t kslot) {
                 constexpr int t = decltype(tc)::value;
-                const uint32_t a0 = q_lo + t * kTile16, b0 = k_lo + kslot * kTile16;
+                const uint32_t a0 = q_lo + t * kTile16, b0 = k_lo + kslot * kSlot16;
 #pragma unroll
                 for (int kk = 0; kk < D / C::kUmmaK; ++kk) {
                     // k step kk: 32 bytes further along the row, next 128-byte atom column
-                    constexpr uint32_t kAtom = C::kChunkBytes >> 4;
-                    const uint32_t off = (uint32_t)((kk * C::kUmmaK) / C::kChunkElems) * kAtom +
-                                         (uint32_t)((kk * 32) % 128 >> 4);
-                    if constexpr (FP8)
-                        umma_f8_ss(tmem_base + 128u * t, desc(a0 + off), desc(b0 + off), C::kIdescQK, kk > 0);
+                    // (a K slot's atom columns are 64 rows deep in a pair)
+                    constexpr uint32_t kAtomA = C::kChunkBytes >> 4, kAtomB = C::kKChunkBytes >> 4;
+                    const uint32_t col = (uint32_t)((kk * C::kUmmaK) / C::kChunkElems);
+                    const uint32_t in_row = (uint32_t)((kk * 32) % 128 >> 4);
+                    const uint32_t a_off = col * kAtomA + in_row, b_off = col * kAtomB + in_row;
+                    if constexpr (PAIR)
+                        umma_f16_ss_pair(tmem_base + 128u * t, desc(a0 + a_off), desc(b0 + b_off), C::kIdescQK,
+                                         kk > 0);
+                    else if constexpr (FP8)
+                        umma_f8_ss(tmem_base + 128u * t, desc(a0 + a_off), desc(b0 + b_off), C::kIdescQK, kk > 0);
                     else
-                        umma_f16_ss(tmem_base + 128u * t, desc(a0 + off), desc(b0 + off), C::kIdescQK, kk > 0);
+                        umma_f16_ss(tmem_base + 128u * t, desc(a0 + a_off), desc(b0 + b_off), C::kIdescQK, kk > 0);
                 }
             };
             // O_t += P_t V : A = P_t from TMEM, B = V (MN-major, 128B-swizzled):
@@ -503,12 +614,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc_pv = (FP8 && p.v_e5m2) ? C::kIdescPV5 : C::kIdescPV;
             auto issue_pv = [&](auto tc, uint32_t vslot, uint32_t acc) {
                 constexpr int t = decltype(tc)::value;
-                const uint32_t b0 = v_lo + vslot * kTile16;
+                const uint32_t b0 = v_lo + vslot * kSlot16;
 #pragma unroll
                 for (int kk = 0; kk < kBN / C::kUmmaK; ++kk) {
                     const uint32_t off = (uint32_t)(kk * C::kUmmaK * 128) >> 4;
                     const uint32_t a_tmem = tmem_base + 128u * t + 8u * kk;
-                    if constexpr (FP8)
+                    if constexpr (PAIR)
+                        umma_f16_ts_pair(tmem_base + C::kColO + 128u * t, a_tmem, desc(b0 + off), C::kIdescPV,
+                                         kk > 0 ? 1u : acc);
+                    else if constexpr (FP8)
                         umma_f8_ts(tmem_base + C::kColO + 128u * t, a_tmem, desc(b0 + off), idesc_pv,
                                    kk > 0 ? 1u : acc);
                     else
@@ -524,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mbar_arrive(bar(C::ITEM_EMPTY + ((items_read - 1) & 1u)));
                 if (w >= p.n_items) break;
-                const Item it = decode_item(p, w);
+                const Item it = decode_item<PAIR>(p, w, rank);
                 if (it.n_hi <= it.n_lo) continue;
                 const int hi0 = it.n_hi_t[0], hi1 = it.n_hi_t[1], lo = it.n_lo;
                 const bool has0 = hi0 > lo, has1 = hi1 > lo;
@@ -541,17 +655,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // (measured: +5 % on FP8, -2 to -4 % on bf16, which releases Q at the item end)
                 if (j0 < hi0) {
                     issue_qk(std::integral_constant<int, 0>{}, kslot0);
-                    umma_commit(bar(C::S_FULL + 0));
-                    if (FP8 && j0 == lo) umma_commit(bar(C::Q_EMPTY + 0));
+                    commit(bar(C::S_FULL + 0));
+                    if (FP8 && j0 == lo) commit(bar(C::Q_EMPTY + 0));
                 } else {
-                    mbar_arrive(bar(C::KV_EMPTY + kslot0));  // tile 0 never reads K(j0)
+                    release_slot(kslot0);  // tile 0 never reads K(j0)
                 }
                 if (j0 < hi1) {
                     issue_qk(std::integral_constant<int, 1>{}, kslot0);
-                    umma_commit(bar(C::S_FULL + 1));
-                    if (FP8 && j0 == lo) umma_commit(bar(C::Q_EMPTY + 1));
+                    commit(bar(C::S_FULL + 1));
+                    if (FP8 && j0 == lo) commit(bar(C::Q_EMPTY + 1));
                 } else {
-                    mbar_arrive(bar(C::KV_EMPTY + kslot0));
+                    release_slot(kslot0);
                 }
                 for (int j = j0; j >= lo; --j) {
                     const uint32_t vslot = ring % C::kStages;
@@ -562,8 +676,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++ring;
                     // a tile that does not visit block j releases V(j) at once (its load has
                     // landed, so the arrival belongs to this phase of the slot)
-                    if (j >= hi0) mbar_arrive(bar(C::KV_EMPTY + vslot));
-                    if (j >= hi1) mbar_arrive(bar(C::KV_EMPTY + vslot));
+                    if (j >= hi0) release_slot(vslot);
+                    if (j >= hi1) release_slot(vslot);
                     const bool has_next = j - 1 >= lo;
                     const uint32_t nslot = ring % C::kStages;  // K(j-1), landed with V(j)
                     if (has_next) ++ring;
@@ -573,10 +687,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const bool cur = j < hi;
                         const bool nxt = has_next && (j - 1) < hi;
                         if (cur) {
-                            if (!wait_bar(bar(C::P_FULL + t), (ph_p >> t) & 1u, wc, SITE_P_FULL)) return false;
+                            if (!wait_handoff(bar(C::P_FULL + t), (ph_p >> t) & 1u, SITE_P_FULL)) return false;
                             ph_p ^= 1u << t;
                             if (acc == 0u &&
-                                !wait_bar(bar(C::O_EMPTY + t), ((ph_o >> t) & 1u) ^ 1u, wc, SITE_O_EMPTY))
+                                !wait_handoff(bar(C::O_EMPTY + t), ((ph_o >> t) & 1u) ^ 1u, SITE_O_EMPTY))
                                 return false;
                             tc_fence_after();
                             issue_pv(tc, vslot, acc);
@@ -584,10 +698,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         if (nxt) {
                             issue_qk(tc, nslot);
-                            umma_commit(bar(C::S_FULL + t));
-                            if (FP8 && j - 1 == lo) umma_commit(bar(C::Q_EMPTY + t));
+                            commit(bar(C::S_FULL + t));
+                            if (FP8 && j - 1 == lo) commit(bar(C::Q_EMPTY + t));
                         } else if (cur) {
-                            umma_commit(bar(C::O_FULL + t));  // last block of tile t
+                            commit(bar(C::O_FULL + t));  // last block of tile t
                         }
                         return true;
                     };
@@ -597,19 +711,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     if (has_next) {  // K(j-1) has landed (some tile read it); skipping tiles release it
-                        if (j - 1 >= hi0) mbar_arrive(bar(C::KV_EMPTY + nslot));
-                        if (j - 1 >= hi1) mbar_arrive(bar(C::KV_EMPTY + nslot));
+                        if (j - 1 >= hi0) release_slot(nslot);
+                        if (j - 1 >= hi1) release_slot(nslot);
                     }
                 }
                 if (aborted) break;
-                if (!FP8 && has0) umma_commit(bar(C::Q_EMPTY + 0));
-                if (!FP8 && has1) umma_commit(bar(C::Q_EMPTY + 1));
+                if (!FP8 && has0) commit(bar(C::Q_EMPTY + 0));
+                if (!FP8 && has1) commit(bar(C::Q_EMPTY + 1));
                 ph_q ^= (has0 ? 1u : 0u) | (has1 ? 2u : 0u);
                 ph_o ^= (has0 ? 1u : 0u) | (has1 ? 2u : 0u);
             }
             // Drain: every MMA issued by this thread has completed before TMEM is
             // released, also after an abort (bounded by the wait limit only).
-            umma_commit(bar(C::DRAIN));
+            if constexpr (PAIR)
+                umma_commit_pair(bar(C::DRAIN));
+            else
+                umma_commit(bar(C::DRAIN));
             if (!mbar_try_wait(bar(C::DRAIN), 0u)) wait_slow(bar(C::DRAIN), 0u, wc, SITE_DRAIN, false);
         }
         __syncwarp();
@@ -639,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::ITEM_EMPTY + ((items_read - 1) & 1u)));
             if (w >= p.n_items) break;
-            const Item it = decode_item(p, w);
+            const Item it = decode_item<PAIR>(p, w, rank);
             if (it.bad_len && r_in_tile == 0 && t == 0) atomicOr(p.err, kErrBadLength);
             const uint32_t item_base = kv_base;
             if (it.n_hi > it.n_lo) kv_base += 2u * (uint32_t)(it.n_hi - it.n_lo);
@@ -842,7 +959,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(C::P_FULL + t));
+                if (lane == 0) {
+                    if constexpr (PAIR)
+                        mbar_arrive_cluster(leader(bar(C::P_FULL + t)));
+                    else
+                        mbar_arrive(bar(C::P_FULL + t));
+                }
             }
             if (aborted) break;
             // ---------------- epilogue: O = O_acc / l, LSE = ln2 * (m + log2 l)
@@ -864,7 +986,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // fixed-length sequence's end fall outside the map and are clipped; a varlen tile
             // that crosses its sequence's end (the next rows belong to another sequence) and
             // the fp32 split partials use plain stores instead.
-            const bool use_tma = !p.split && (!p.varlen || t_m0 + kBM <= it.sq * p.pack);
+            // (in a pair, the odd CTA's tile of the last slot may lie wholly past the end)
+            const bool use_tma = !p.split && t_m0 < it.sq * p.pack &&
+                                 (!p.varlen || t_m0 + kBM <= it.sq * p.pack);
             if (use_tma) {
                 const uint32_t srow = s_base + C::kStageOff + (uint32_t)t * C::kStageBytes +
                                       (uint32_t)r_in_tile * 128u;
@@ -940,7 +1064,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::O_EMPTY + t));
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    mbar_arrive_cluster(leader(bar(C::O_EMPTY + t)));
+                else
+                    mbar_arrive(bar(C::O_EMPTY + t));
+            }
             if (row_ok)
                 *lse_ptr = has_mass ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
         }
@@ -948,48 +1077,92 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // the TMA stores of O have completed before this CTA retires (their issuing threads wait)
     if (warp >= 4 && (threadIdx.x & (kBM - 1)) == 0) bulk_wait_group0();
-    __syncthreads();
+    // a pair retires together: the even CTA's MMAs (drained above) no longer read the odd
+    // CTA's shared memory or write its TMEM, and no load or arrival of one CTA is still
+    // heading for the other's barriers
+    if constexpr (PAIR) {
+        __syncwarp();
+        cluster_sync();
+    } else {
+        __syncthreads();
+    }
     // lets a programmatically dependent grid (the split merge) be scheduled; it still
     // waits for this grid's completion before reading anything
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool PAIR = false>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t stream,
                        bool after_append) {
-    using C = Cfg<D, FP8>;
+    using C = Cfg<D, FP8, PAIR>;
     static bool attr_done = false;  // per process; the attribute is per function
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, FP8>,
+        cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, FP8, PAIR>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    if (!after_append) {
-        fa_fwd_kernel<D, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, o, p);
+    if (!after_append && !PAIR) {
+        fa_fwd_kernel<D, FP8, PAIR><<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, o, p);
         return cudaGetLastError();
     }
     // after the cache append: programmatic dependent launch, so this grid's set-up
     // (barriers, TMEM, descriptor prefetch) overlaps the append; the producer waits for
-    // the append's completion (griddepcontrol.wait) before its first load
+    // the append's completion (griddepcontrol.wait) before its first load.
+    // CTA pairs: clusters of two CTAs (grid = 2 x pairs)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (after_append) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (PAIR) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, FP8, PAIR>, q, k, v, o, p);
+}
+
+// How many CTA pairs of the kernel can be resident at once (0 if none).
+template <int D, bool FP8>
+cudaError_t max_resident_pairs(int* pairs) {
+    using C = Cfg<D, FP8, true>;
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, FP8, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2u);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, FP8>, q, k, v, o, p);
+    return cudaOccupancyMaxActiveClusters(pairs, fa_fwd_kernel<D, FP8, true>, &cfg);
 }
 
 }  // namespace fa

@@ -33,7 +33,8 @@ struct FwdParams {
     int item_heads;             // heads the items run over: heads, or heads / pack
     int seqlen_q, seqlen_k;     // fixed length: the lengths; varlen: max lengths
     int total_q;                // varlen: packed rows of Q (LSE row stride)
-    int n_mpairs;               // ceil(seqlen_q * pack / 256): (packed) row pairs of tiles
+    int n_mpairs;               // ceil(seqlen_q * pack / 256) (packed) row pairs of tiles;
+                                //   CTA pairs: ceil(seqlen_q / 512) groups of four tiles
     int n_splits;               // key-range splits (1 = none)
     int blocks_per_split;       // key blocks per split
     int n_items;                // n_mpairs * batch * item_heads * n_splits
@@ -59,6 +60,12 @@ cudaError_t launch_fwd_bf16_d128(const CUtensorMap& q, const CUtensorMap& k, con
 cudaError_t launch_fwd_e4m3_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                  const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t s,
                                 bool after_append);
+// CTA-pair variant (bf16, D = 128; no packing, splits or cache lengths): grid = 2 x pairs,
+// launched as clusters of two; k is a map with 64-row boxes (half a key block)
+cudaError_t launch_fwd_pair_bf16_d128(const CUtensorMap& q, const CUtensorMap& k,
+                                      const CUtensorMap& v, const CUtensorMap& o,
+                                      const FwdParams& p, int grid, cudaStream_t s);
+cudaError_t max_resident_pairs_bf16_d128(int* pairs);
 cudaError_t launch_append_kv(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                              const int32_t* cache_seqlens, int batch, int capacity, int n_new,
                              long long row_bytes, uint32_t* err, cudaStream_t s);

@@ -157,6 +157,31 @@ FA_API fa_status fa_fwd_fp8(const void* q, const void* k, const void* v,
                             void* stream);
 
 /*
+ * fa_fwd_2cta -- the bf16 forward pass of fa_fwd_gqa computed by the CTA-pair
+ * kernel: clusters of two CTAs on two SMs run 256-row tcgen05 MMAs
+ * (cta_group::2), each CTA loading its own query rows and one half of every K/V
+ * block (64 keys of K, 64 head-dim columns of V), so each SM streams half of the
+ * K/V bytes through shared memory.  The page "Dissecting the SM_120
+ * Microarchitecture" (section 4, feature matrix Fig. 1) lists this 2-SM
+ * cooperative MMA among the SM_100-class features; the attention it computes is
+ * that of fa_fwd.
+ *   q, k, v, o, lse, batch, heads, heads_k, seqlen_q/k, cu_seqlens_q/k,
+ *   max_seqlen_q/k, softmax_scale, causal, stream: as fa_fwd_gqa (bf16 only,
+ *   head_dim = head_dim_v = 128, no workspace: no key splits).
+ * Same outputs, layouts and validation as fa_fwd_gqa.  FA_ERR_UNSUPPORTED for
+ * head_dim != 128, or when no cluster of two CTAs fits on the device.  The
+ * work items (512 query rows of one batch and head) follow a static
+ * longest-first order, also for varlen.
+ */
+FA_API fa_status fa_fwd_2cta(const void* q, const void* k, const void* v,
+                             void* o, float* lse,
+                             int batch, int heads, int heads_k, int seqlen_q, int seqlen_k,
+                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                             int max_seqlen_q, int max_seqlen_k,
+                             int head_dim, float softmax_scale, int causal,
+                             void* stream);
+
+/*
  * fa_fwd_kvcache -- append new key/value rows to a key/value cache, then attend
  * over the cache.  The AppendKV branch of the producer loop on the page
  * "FlashAttention core algorithm: forward pass" (scheduler-loop excerpt) loads

@@ -29,13 +29,13 @@ def to_dev(x, dev="cuda"):
     return out
 
 
-def run_gpu(x, *, causal, softmax_scale, workspace="auto"):
+def run_gpu(x, *, causal, softmax_scale, workspace="auto", cta_pair=False):
     d = to_dev(x)
     o, lse = fa.fwd(d["q"], d["k"], d["v"], causal=causal, softmax_scale=softmax_scale,
                     cu_seqlens_q=d.get("cu_seqlens_q"), cu_seqlens_k=d.get("cu_seqlens_k"),
                     max_seqlen_q=x.get("max_seqlen_q"), max_seqlen_k=x.get("max_seqlen_k"),
                     descale=x["descale"] if x["q"].dtype == torch.float8_e4m3fn else None,
-                    workspace=workspace)
+                    workspace=workspace, cta_pair=cta_pair)
     torch.cuda.synchronize()
     st, flags = fa.device_error(clear=True)
     assert st == 0, f"device error word {flags:#x}"

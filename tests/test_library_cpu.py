@@ -154,3 +154,27 @@ def test_kvcache_validation(lib, kw, code):
 
 def test_kvcache_empty_batch_is_ok_without_a_device(lib):
     assert kvc(lib, batch=0) == fa.FA_OK
+
+
+def pair(lib, **kw):
+    a = dict(batch=1, heads=4, heads_k=2, sq=128, sk=128, d=128, scale=0.1, causal=1, q=P)
+    a.update(kw)
+    return lib.fa_fwd_2cta(a["q"], P, P, P, P, a["batch"], a["heads"], a["heads_k"], a["sq"],
+                           a["sk"], None, None, 0, 0, a["d"], a["scale"], a["causal"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(heads_k=3), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=3), fa.FA_ERR_INVALID_ARG),
+    (dict(d=64), fa.FA_ERR_UNSUPPORTED),               # the CTA-pair kernel is built for D = 128
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+])
+def test_cta_pair_validation(lib, kw, code):
+    assert pair(lib, **kw) == code
+    assert lib.fa_last_error_detail()
+
+
+def test_cta_pair_empty_problem_is_ok_without_a_device(lib):
+    assert pair(lib, batch=0) == fa.FA_OK
