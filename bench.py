@@ -1,6 +1,6 @@
 """Benchmark of the attention forward pass on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--cta-pair]
     python bench.py --impl reference ...     # the fp64 CPU oracle, timed on host cores
 
 Prints ONE JSON line (rank 0).  A step is one forward pass over the whole
@@ -346,7 +346,10 @@ def run_gpu(args, w):
     lse_shape = (w.batch, w.heads, w.seqlen_q) if not w.varlen else (w.heads, q.shape[0])
     lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
     ws = None
-    if not w.varlen:
+    pair = bool(getattr(args, "cta_pair", False))
+    if pair and (fp8 or w.head_dim != 128 or w.cache_new):
+        raise SystemExit("--cta-pair runs the bf16 head-dim-128 attention workloads only")
+    if not w.varlen and not pair:
         need = fa.workspace_size(w.batch, w.heads, w.seqlen_q, w.seqlen_k, w.head_dim, w.causal,
                                  heads_k=w.kv_heads)
         if need:
@@ -371,7 +374,7 @@ def run_gpu(args, w):
             return
         fa.fwd(q, k, v, causal=w.causal, softmax_scale=w.softmax_scale, cu_seqlens_q=cu_q,
                cu_seqlens_k=cu_k, max_seqlen_q=x["max_seqlen_q"], max_seqlen_k=x["max_seqlen_k"],
-               descale=descale, workspace=ws, out=o, lse=lse, stream=stream)
+               descale=descale, workspace=ws, out=o, lse=lse, stream=stream, cta_pair=pair)
 
     for _ in range(args.warmup):
         flush_l2()
@@ -445,7 +448,7 @@ def run_gpu(args, w):
                 fa.fwd(d["q"], d["k"], d["v"], causal=w.causal, softmax_scale=w.softmax_scale,
                        cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=x["max_seqlen_q"],
                        max_seqlen_k=x["max_seqlen_k"], descale=descale, workspace=ws, out=oo,
-                       lse=ll, stream=stream)
+                       lse=ll, stream=stream, cta_pair=pair)
             ev_comp[bi].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_comp[bi])
@@ -501,7 +504,8 @@ def run_gpu(args, w):
         src = f"{peak_src} MEASURED_PEAKS.json burst" + (
             " x2 (fp8/bf16 nominal ratio)" if fp8 and bound == "tensor" else "")
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": _recorded_traffic(w.name),
+                "frac": achieved / peak,
+                "traffic": _recorded_traffic(w.name + ("/cta_pair" if pair else "")),
                 "peak_source": src,
                 "frac_of_sustained": (achieved / peaks.get("bf16_tflops_sustained", peak)
                                       if bound == "tensor" and not fp8 else None)}
@@ -511,7 +515,8 @@ def run_gpu(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if not fp8 else "e4m3", "data": "synthetic",
-        "config": _config(w, "flushed between timed steps (256 MiB write + 256 MiB read, untimed)"),
+        "config": dict(_config(w, "flushed between timed steps (256 MiB write + 256 MiB read, untimed)"),
+                       kernel="cta_pair (clusters of 2, cta_group::2)" if pair else "one CTA per SM"),
         "clocks": clocks, "e2e": e2e,
         "gpu_launches": args.steps * ((2 if splits > 1 else 1) + (1 if cache is not None else 0)),
         "roofline": roofline,
@@ -543,6 +548,8 @@ def main(argv=None):
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cta-pair", action="store_true",
+                    help="time the CTA-pair kernel (fa_fwd_2cta) instead of the one-CTA kernel")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
