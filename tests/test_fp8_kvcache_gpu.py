@@ -157,6 +157,24 @@ def test_kvcache_append_and_attend(B, H, Hk, Sq, cap, lens, n_new, causal):
             o_ref, lse_ref, what=f"kvcache {(B, H, Hk, Sq, cap, lens, n_new, causal)}")
 
 
+def test_kvcache_decode_many_items():
+    # 16 sequences x 8 K/V heads = 128 packed decode items (one per CTA, no key splits);
+    # lengths include empty, one row, a full cache, block edges and random ones
+    B, H, Hk, Sq, cap, n_new = 16, 32, 8, 1, 2048, 1
+    rng = np.random.default_rng(350)
+    lens = [0, 1, cap - 1, 127, 128, 129] + [int(v) for v in rng.integers(0, cap, size=B - 6)]
+    xc, new, lens_t = _cache_case(B, H, Hk, Sq, cap, lens, n_new, seed=350)
+    o, lse, kc, vc = _run_cache(xc, new, lens_t, True)
+    st, flags = fa.device_error(clear=True)
+    assert st == fa.FA_OK, f"device error word {flags:#x}"
+    k_ref = oracle.append_kv(xc["k"], new[0], lens)
+    v_ref = oracle.append_kv(xc["v"], new[1], lens)
+    o_ref, lse_ref = oracle.attention(xc["q"], k_ref, v_ref, softmax_scale=128 ** -0.5,
+                                      causal=True, seqused_k=[l + n_new for l in lens])
+    compare(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+            o_ref, lse_ref, what="kvcache decode, 128 items")
+
+
 def test_kvcache_fp8_head_descales_e5m2_v():
     B, H, Hk, Sq, cap, lens, n_new = 2, 8, 2, 64, 3000, [1000, 2500], 64
     xc, new, lens_t = _cache_case(B, H, Hk, Sq, cap, lens, n_new, seed=333, dtype="e4m3",
