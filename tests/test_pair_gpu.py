@@ -115,3 +115,23 @@ def test_pair_rejects_unbuilt_configurations():
     q8 = torch.zeros(1, 128, 2, 128, device="cuda").to(torch.float8_e4m3fn)
     with pytest.raises(ValueError):
         fa.fwd(q8, q8, q8, cta_pair=True)
+
+
+def test_pair_bounded_wait_timeout_is_reported_and_context_survives():
+    # both CTAs of each pair withhold their Q loads: the even CTA's MMA issuer gives up on
+    # its Q barrier, every role of both CTAs leaves through a bounded wait, the pair meets
+    # at the closing cluster barrier and frees its TMEM together
+    x = inputs.make_random(1, 2, 600, 600, 128, seed=341)
+    fa.device_error(clear=True)
+    fa.debug_set(wait_limit_ns=200_000_000, inject=1)
+    try:
+        d = {n: x[n].cuda() for n in "qkv"}
+        fa.fwd(d["q"], d["k"], d["v"], causal=True, cta_pair=True)
+        st, flags = fa.device_error(clear=True)
+    finally:
+        fa.debug_set(0, 0)
+    assert st == fa.FA_ERR_DEVICE_TIMEOUT and flags & 1
+    # the context is still usable and the pair kernel's results are right again
+    o, lse = run_gpu(x, causal=True, softmax_scale=128 ** -0.5, cta_pair=True)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=128 ** -0.5, causal=True)
+    compare(o, lse, o_ref, lse_ref, what="pair after timeout")
