@@ -167,7 +167,9 @@ size_t workspace_bytes_for(int splits, int batch, int heads, int sq, int dv) {
 // One warp per output row.  LSE = ln sum_s exp(LSE_s) and O = sum_s exp(LSE_s - LSE) O_s.
 // Lanes own splits for the LSE reductions (warp shuffles; for <= 32 splits each lane keeps
 // its weight in a register and broadcasts it), then own 4 (Dv = 128) or 2 (Dv = 64)
-// columns of O; the split loop is unrolled so several partial rows are in flight at once.
+// columns of O.  The partial rows of the first batch of splits are requested together
+// with the LSEs (they do not depend on the weights), and a batch holds 12 splits, so up
+// to 12 splits take one memory round trip and up to 24 take two.
 template <int DV>
 __global__ void __launch_bounds__(256) fa_combine_kernel(const float* __restrict__ ws_o,
                                                          const float* __restrict__ ws_lse,
@@ -175,6 +177,7 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const float* __restrict
                                                          float* __restrict__ lse, int batch,
                                                          int heads, int sq, int splits) {
     constexpr int kCols = DV / 32;  // columns per lane
+    constexpr int kBatch = 12;
     const long long rows = (long long)batch * heads * sq;
     const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -184,38 +187,12 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const float* __restrict
     const int h = (int)(bh % heads);
     const long long b = bh / heads;
     const size_t stride = (size_t)rows;  // rows per split
+    const float* src = ws_o + (size_t)row * DV + lane * kCols;
     // launched as a programmatic dependent of the forward kernel: wait for its
     // completion (and memory) before reading the partial results
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    float mx = -INFINITY;
-    for (int s = lane; s < splits; s += 32) mx = fmaxf(mx, __ldg(ws_lse + s * stride + row));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    __nv_bfloat16* out = o + (((size_t)b * sq + i) * heads + h) * DV + lane * kCols;
-    float* lse_out = lse + ((size_t)b * heads + h) * sq + i;
-    if (mx == -INFINITY) {  // no split saw a key: O = 0, LSE = -inf
-#pragma unroll
-        for (int c = 0; c < kCols; ++c) out[c] = __float2bfloat16(0.f);
-        if (lane == 0) *lse_out = -INFINITY;
-        return;
-    }
-    float w_lane = 0.f, tot = 0.f;
-    for (int s = lane; s < splits; s += 32) {
-        const float e = expf(__ldg(ws_lse + s * stride + row) - mx);
-        if (s < 32) w_lane = e;
-        tot += e;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-    const float inv = 1.0f / tot;
-    float acc[kCols];
-#pragma unroll
-    for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
-    const float* src = ws_o + (size_t)row * DV + lane * kCols;
-    // batches of 8 splits: all 8 partial-row loads are issued before any is used
-    constexpr int kBatch = 8;
-    for (int s0 = 0; s0 < splits; s0 += kBatch) {
-        float v[kBatch][kCols];
+    // partial rows of splits [s0, s0 + kBatch): all loads issued before any is used
+    auto load_batch = [&](int s0, float (&v)[kBatch][kCols]) {
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int s = s0 + u;
@@ -231,6 +208,33 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const float* __restrict
                 }
             }
         }
+    };
+    const float lse_lane = lane < splits ? __ldg(ws_lse + lane * stride + row) : -INFINITY;
+    float v[kBatch][kCols];
+    load_batch(0, v);
+    float mx = lse_lane;
+    for (int s = lane + 32; s < splits; s += 32) mx = fmaxf(mx, __ldg(ws_lse + s * stride + row));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    __nv_bfloat16* out = o + (((size_t)b * sq + i) * heads + h) * DV + lane * kCols;
+    float* lse_out = lse + ((size_t)b * heads + h) * sq + i;
+    if (mx == -INFINITY) {  // no split saw a key: O = 0, LSE = -inf
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) out[c] = __float2bfloat16(0.f);
+        if (lane == 0) *lse_out = -INFINITY;
+        return;
+    }
+    const float w_lane = lane < splits ? expf(lse_lane - mx) : 0.f;
+    float tot = w_lane;
+    for (int s = lane + 32; s < splits; s += 32) tot += expf(__ldg(ws_lse + s * stride + row) - mx);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+    const float inv = 1.0f / tot;
+    float acc[kCols];
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
+    for (int s0 = 0; s0 < splits; s0 += kBatch) {
+        if (s0 > 0) load_batch(s0, v);
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int s = s0 + u;  // uniform across the warp
