@@ -72,6 +72,7 @@
 
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "fa_internal.h"
@@ -1104,13 +1105,17 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
                        const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t stream,
                        bool after_append) {
     using C = Cfg<D, FP8, PAIR>;
-    static bool attr_done = false;  // per process; the attribute is per function
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, FP8, PAIR>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::kSmemBytes);
+    // The shared-memory attribute is set once per device (devices 0-63; others every
+    // launch): an atomic flag per device, so concurrent host threads at worst set it twice.
+    static std::atomic<bool> attr_done[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(fa_fwd_kernel<D, FP8, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_done = true;
+        if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
     }
     if (!after_append && !PAIR) {
         fa_fwd_kernel<D, FP8, PAIR><<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, o, p);
