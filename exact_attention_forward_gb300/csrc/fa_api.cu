@@ -400,6 +400,9 @@ fa_status fwd_impl(const FwdArgs& a) {
     p.heads = a.heads;
     p.kv_group = a.heads / a.heads_k;
     p.pack = pack;
+    p.pack_shift = 0;
+    while ((1 << p.pack_shift) < pack) ++p.pack_shift;
+    if ((1 << p.pack_shift) != pack) return fail(FA_ERR_INVALID_ARG, "internal: pack %d", pack);
     p.item_heads = a.heads / pack;
     p.seqlen_q = mq;
     p.seqlen_k = mk;

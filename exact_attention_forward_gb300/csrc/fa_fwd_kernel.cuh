@@ -143,7 +143,10 @@ struct Cfg {
         KV_EMPTY = 21 + kStages, NUM_BARS = 21 + 2 * kStages
     };
     static constexpr int kMiscOff = kBarOff + NUM_BARS * 8;
-    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1 KiB
+    // misc: TMEM address, abort flag, item ring indices (16 B); then the two decoded item
+    // records of the ring (64 B each, 16-byte aligned)
+    static constexpr int kItemRecOff = (kMiscOff + 16 + 15) / 16 * 16;
+    static constexpr int kSmemBytes = kItemRecOff + 2 * 64 + 1024;  // + slack to align the base to 1 KiB
     static constexpr int kMmaM = PAIR ? 2 * kBM : kBM;  // rows of one MMA (both CTAs of a pair)
     static constexpr uint32_t kIdescQK = make_idesc(kMmaM, kBN, 0u + (FP8 ? 0u : 1u), false);
     static constexpr uint32_t kIdescPV = make_idesc(kMmaM, D, 0u + (FP8 ? 0u : 1u), true);
@@ -228,6 +231,27 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int w, uint32_t 
     return it;
 }
 
+// The producer decodes each item once and passes it to the other roles in a 64-byte
+// shared-memory record (sixteen 32-bit words), next to the index in the item ring.
+__device__ __forceinline__ void store_item(uint8_t* rec, int w, const Item& it) {
+    int4* r = reinterpret_cast<int4*>(rec);
+    const int flags = (it.active[0] ? 1 : 0) | (it.active[1] ? 2 : 0) | (it.bad_len ? 4 : 0);
+    r[0] = make_int4(w, it.b, it.h, it.split);
+    r[1] = make_int4(it.sq, it.sk, it.q_row0, it.k_row0);
+    r[2] = make_int4(it.m0[0], it.m0[1], it.n_lo, it.n_hi);
+    r[3] = make_int4(it.n_hi_t[0], it.n_hi_t[1], flags, 0);
+}
+__device__ __forceinline__ int load_item(const uint8_t* rec, Item& it) {
+    const int4* r = reinterpret_cast<const int4*>(rec);
+    const int4 a = r[0], b = r[1], c = r[2], d = r[3];
+    it.b = a.y; it.h = a.z; it.split = a.w;
+    it.sq = b.x; it.sk = b.y; it.q_row0 = b.z; it.k_row0 = b.w;
+    it.m0[0] = c.x; it.m0[1] = c.y; it.n_lo = c.z; it.n_hi = c.w;
+    it.n_hi_t[0] = d.x; it.n_hi_t[1] = d.y;
+    it.active[0] = (d.z & 1) != 0; it.active[1] = (d.z & 2) != 0; it.bad_len = (d.z & 4) != 0;
+    return a.x;
+}
+
 // Which item a CTA takes next is decided by its producer thread, which passes the
 // index to the MMA issuer and the softmax warps through a two-entry ring in shared
 // memory (ITEM_FULL / ITEM_EMPTY mbarriers), published once the current item's loads
@@ -303,7 +327,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_bar = s_base + C::kBarOff;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 4);
-    volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 8);  // 2 entries
     auto bar = [&](int i) -> uint32_t { return s_bar + 8u * (uint32_t)i; };
 
     const int warp = threadIdx.x >> 5;
@@ -366,10 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtx wc{p.wait_limit_ns, p.err, abort_flag};
     // consumer side of the item ring: the next item index (n_items = no more work)
     uint32_t items_read = 0;
-    auto read_item = [&](int& w) -> bool {
+    // (the index, and for an index below p.n_items the decoded item)
+    auto read_item = [&](int& w, Item& it) -> bool {
         const uint32_t slot = items_read & 1u;
         if (!wait_bar(bar(C::ITEM_FULL + slot), (items_read >> 1) & 1u, wc, SITE_ITEM_FULL)) return false;
-        w = item_ring[slot];
+        w = load_item(smem + C::kItemRecOff + 64 * slot, it);
         ++items_read;
         return true;
     };
@@ -393,13 +417,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool withheld = false;
             bool aborted = false;
             uint32_t published = 0;
-            auto publish = [&](int w) -> bool {
+            // decodes item w (an index below p.n_items) into `it` and publishes both
+            auto publish = [&](int w, Item& it) -> bool {
                 const uint32_t slot = published & 1u;
+                if (w < p.n_items) it = decode_item<PAIR>(p, w, rank);
                 if (published >= 2 &&
                     !wait_bar(bar(C::ITEM_EMPTY + slot), ((published >> 1) - 1) & 1u, wc, SITE_ITEM_EMPTY))
                     return false;
-                item_ring[slot] = w;
-                mbar_arrive(bar(C::ITEM_FULL + slot));  // release: the index is visible to waiters
+                store_item(smem + C::kItemRecOff + 64 * slot, w, it);
+                mbar_arrive(bar(C::ITEM_FULL + slot));  // release: the record is visible to waiters
                 ++published;
                 return true;
             };
@@ -419,13 +445,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool greedy = !PAIR && p.greedy;
             int w_next = unit;
             int round_no = 0;  // static order: rounds of the snake
-            if (!publish(w_next)) aborted = true;
+            Item it_next{};
+            if (!publish(w_next, it_next)) aborted = true;
             for (int w = w_next; !aborted && w < p.n_items; w = w_next) {
                 // the next index is requested now and published once this item's loads have
                 // been issued, so the counter's round trip overlaps them
                 ++round_no;
                 const uint32_t ticket = greedy ? atomicAdd(p.sched, 1u) : 0u;
-                const Item it = decode_item<PAIR>(p, w, rank);
+                const Item it = it_next;
                 const int bc = p.varlen ? 0 : it.b;  // batch coordinate of the 4-D view
                 auto load_q = [&](auto tc) -> bool {
                     constexpr int t = decltype(tc)::value;
@@ -527,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     w_next = min(item_of_round(round_no, unit, nunits), p.n_items);
                 }
-                if (!publish(w_next)) {
+                if (!publish(w_next, it_next)) {
                     aborted = true;
                     break;
                 }
@@ -550,7 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the odd CTA of a pair issues nothing; it only keeps its item ring turning
             for (;;) {
                 int w;
-                if (!read_item(w)) break;
+                Item it;
+                if (!read_item(w, it)) break;
                 mbar_arrive(bar(C::ITEM_EMPTY + ((items_read - 1) & 1u)));
                 if (w >= p.n_items) break;
             }
@@ -633,13 +661,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             for (;;) {
                 int w;
-                if (!read_item(w)) {
+                Item it;
+                if (!read_item(w, it)) {
                     aborted = true;
                     break;
                 }
                 mbar_arrive(bar(C::ITEM_EMPTY + ((items_read - 1) & 1u)));
                 if (w >= p.n_items) break;
-                const Item it = decode_item<PAIR>(p, w, rank);
                 if (it.n_hi <= it.n_lo) continue;
                 const int hi0 = it.n_hi_t[0], hi1 = it.n_hi_t[1], lo = it.n_lo;
                 const bool has0 = hi0 > lo, has1 = hi1 > lo;
@@ -746,18 +774,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t kv_base = 0;  // ring position of the current item's first K/V load
         const bool releaser = wq == 0 && lane == 0;  // this warpgroup's slot-release thread
         bool aborted = false;
+        uint32_t held = 0;  // 1 + the item-ring slot whose record this warp still reads (0: none)
+        bool stg_owed = false;  // (thread 0 of the tile) its last O store's read is unconfirmed
+        // output addresses of this thread's row of a tile starting at (packed) row m0 of the
+        // item (b, h, split, first packed row q_row0); false past the sequence end
+        auto out_addr = [&](int b, int h, int split, int q_row0, int sq, int m0, float*& lse_ptr,
+                            float*& wso_ptr, __nv_bfloat16*& o_ptr) -> bool {
+            const int prow = m0 + r_in_tile;               // (packed) tile row
+            const int row = prow >> p.pack_shift;           // query row within the sequence
+            const int hrow = h + (prow & (p.pack - 1));     // query head of this row
+            wso_ptr = nullptr;
+            o_ptr = nullptr;
+            if (p.split) {
+                const size_t rid = (((size_t)split * p.batch + b) * p.heads + hrow) * (size_t)p.seqlen_q + row;
+                lse_ptr = p.ws_lse + rid;
+                wso_ptr = p.ws_o + rid * D;
+            } else if (p.varlen) {
+                lse_ptr = p.lse + (size_t)hrow * p.total_q + q_row0 + row;
+                o_ptr = reinterpret_cast<__nv_bfloat16*>(p.o) + (((size_t)q_row0 + row) * p.heads + hrow) * D;
+            } else {
+                lse_ptr = p.lse + ((size_t)b * p.heads + hrow) * p.seqlen_q + row;
+                o_ptr = reinterpret_cast<__nv_bfloat16*>(p.o) + (((size_t)b * p.seqlen_q + row) * p.heads + hrow) * D;
+            }
+            return prow < (sq << p.pack_shift);
+        };
         for (;;) {
             int w = 0;
-            bool got = read_item(w);
+            Item it;
+            bool got = read_item(w, it);
             got = __all_sync(0xffffffffu, got);
             if (!got) {
                 aborted = true;
                 break;
             }
+            // The previous item is finished: release its record.  This item's record is held
+            // until then -- its epilogue reads its output coordinates back from it rather than
+            // keeping them in registers through the key loop.  (The producer reuses a slot
+            // only after issuing every load of the item in between.)
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::ITEM_EMPTY + ((items_read - 1) & 1u)));
+            if (lane == 0 && held) mbar_arrive(bar(C::ITEM_EMPTY + (held - 1u)));
+            held = 1u + ((items_read - 1) & 1u);
             if (w >= p.n_items) break;
-            const Item it = decode_item<PAIR>(p, w, rank);
             if (it.bad_len && r_in_tile == 0 && t == 0) atomicOr(p.err, kErrBadLength);
             const uint32_t item_base = kv_base;
             if (it.n_hi > it.n_lo) kv_base += 2u * (uint32_t)(it.n_hi - it.n_lo);
@@ -780,29 +837,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 scale_log2 *= qd * kd;
                 o_scale = p.v_descale ? __ldg(p.v_descale + ds) : 1.0f;
             }
-            const int prow = t_m0 + r_in_tile;          // this thread's (packed) tile row
-            const int row = prow / p.pack;               // query row within the sequence
-            const int hrow = it.h + prow % p.pack;       // query head of this row
-            const bool row_ok = prow < it.sq * p.pack;
-            // output addresses
-            float* lse_ptr;
-            float* wso_ptr = nullptr;
-            __nv_bfloat16* o_ptr = nullptr;
-            if (p.split) {
-                const size_t rid =
-                    (((size_t)it.split * p.batch + it.b) * p.heads + hrow) * (size_t)p.seqlen_q + row;
-                lse_ptr = p.ws_lse + rid;
-                wso_ptr = p.ws_o + rid * D;
-            } else if (p.varlen) {
-                lse_ptr = p.lse + (size_t)hrow * p.total_q + it.q_row0 + row;
-                o_ptr = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                        (((size_t)it.q_row0 + row) * p.heads + hrow) * D;
-            } else {
-                lse_ptr = p.lse + ((size_t)it.b * p.heads + hrow) * p.seqlen_q + row;
-                o_ptr = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                        (((size_t)it.b * p.seqlen_q + row) * p.heads + hrow) * D;
-            }
+            const int row = (t_m0 + r_in_tile) >> p.pack_shift;  // query row within the sequence
             if (t_hi <= it.n_lo) {
+                float* lse_ptr;
+                float* wso_ptr;
+                __nv_bfloat16* o_ptr;
+                const bool row_ok =
+                    out_addr(it.b, it.h, it.split, it.q_row0, it.sq, t_m0, lse_ptr, wso_ptr, o_ptr);
                 // no visible key for any row of this tile: O = 0, LSE = -inf
                 if (row_ok) {
                     if (p.split) {
@@ -819,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // visible keys of this row: [0, vis_end) with vis_end = min(sk, row + sk - sq + 1)
             const int vis_end = p.causal ? min(it.sk, row + it.sk - it.sq + 1) : it.sk;
             // a block needs masking iff some column of it is invisible to some row of the tile
-            const int tile_rmin = t_m0 / p.pack;  // the tile's first query row
+            const int tile_rmin = t_m0 >> p.pack_shift;  // the tile's first query row
             const int tile_vis_min = p.causal ? min(it.sk, tile_rmin + it.sk - it.sq + 1) : it.sk;
             float m_run = -INFINITY;  // running max of scale_log2 * s (lazy reference)
             float l_run = 0.0f;       // running sum of exp2(scale_log2 * s - m_run)
@@ -982,60 +1023,98 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (releaser) mbar_arrive(bar(C::KV_EMPTY + v_slot(it.n_lo)));  // PV_t(n_lo) is complete
             const bool has_mass = l_run > 0.0f;
             const float inv_l = has_mass ? o_scale / l_run : 0.0f;
+            // output coordinates, read back from this item's record
+            Item io;
+            load_item(smem + C::kItemRecOff + 64 * (held - 1u), io);
+            const int o_m0 = t ? io.m0[1] : io.m0[0];
+            float* lse_ptr;
+            float* wso_ptr;
+            __nv_bfloat16* o_ptr;
+            const bool row_ok =
+                out_addr(io.b, io.h, io.split, io.q_row0, io.sq, o_m0, lse_ptr, wso_ptr, o_ptr);
             // The O tile goes out by TMA store from a per-tile staging buffer (128 rows x 64
             // columns, 128-byte swizzled like the tensor map), in D / 64 passes.  Rows past a
             // fixed-length sequence's end fall outside the map and are clipped; a varlen tile
             // that crosses its sequence's end (the next rows belong to another sequence) and
             // the fp32 split partials use plain stores instead.
             // (in a pair, the odd CTA's tile of the last slot may lie wholly past the end)
-            const bool use_tma = !p.split && t_m0 < it.sq * p.pack &&
-                                 (!p.varlen || t_m0 + kBM <= it.sq * p.pack);
+            const int sq_rows = io.sq << p.pack_shift;
+            const bool use_tma = !p.split && o_m0 < sq_rows && (!p.varlen || o_m0 + kBM <= sq_rows);
             if (use_tma) {
-                const uint32_t srow = s_base + C::kStageOff + (uint32_t)t * C::kStageBytes +
-                                      (uint32_t)r_in_tile * 128u;
+                // O leaves TMEM first (normalised and packed to bf16 on the way), so the MMA
+                // issuer gets it back (O_EMPTY) before any staging
+                uint32_t pk[D / 2];
+#pragma unroll
+                for (int hh = 0; hh < D / 64; ++hh) {
+                    uint32_t o0[32], o1[32];
+                    tmem_ld32(t_o + hh * 64, o0);
+                    tmem_ld32(t_o + hh * 64 + 32, o1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        pk[hh * 32 + i] = pack_bf16x2(__uint_as_float(o0[2 * i]) * inv_l,
+                                                      __uint_as_float(o0[2 * i + 1]) * inv_l);
+                        pk[hh * 32 + 16 + i] = pack_bf16x2(__uint_as_float(o1[2 * i]) * inv_l,
+                                                           __uint_as_float(o1[2 * i + 1]) * inv_l);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (PAIR)
+                        mbar_arrive_cluster(leader(bar(C::O_EMPTY + t)));
+                    else
+                        mbar_arrive(bar(C::O_EMPTY + t));
+                }
+                // the last store of the previous epilogue out of this buffer: its issuing
+                // thread confirms that the TMA engine has read it only now, when the buffer is
+                // needed again, instead of waiting for it at the end of that epilogue
+                if (r_in_tile == 0 && stg_owed) {
+                    bulk_wait_group_read0();
+                    mbar_arrive(bar(C::STG_EMPTY + t));
+                    stg_owed = false;
+                }
+                const uint32_t stile = s_base + C::kStageOff + (uint32_t)t * C::kStageBytes;
+                const uint32_t srow = stile + (uint32_t)r_in_tile * 128u;
                 const uint32_t sw = (uint32_t)(r_in_tile & 7);
-#pragma unroll 1
+                bool bad = false;
+#pragma unroll
                 for (int hh = 0; hh < D / 64; ++hh) {
                     // the previous store out of this buffer has read it
                     if (stg_cnt > 0 &&
-                        !wait_bar(bar(C::STG_EMPTY + t), (stg_cnt - 1) & 1u, wc, SITE_STG_EMPTY)) {
-                        aborted = true;
-                    }
-                    if (__any_sync(0xffffffffu, aborted)) break;
+                        !wait_bar(bar(C::STG_EMPTY + t), (stg_cnt - 1) & 1u, wc, SITE_STG_EMPTY))
+                        bad = true;
+                    if (__any_sync(0xffffffffu, bad)) break;
+                    // 16-byte chunk c of the row lands at chunk c ^ (row mod 8)
 #pragma unroll
-                    for (int c2 = 0; c2 < 2; ++c2) {
-                        uint32_t orr[32];
-                        tmem_ld32(t_o + hh * 64 + c2 * 32, orr);
-                        tmem_wait_ld();
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pk[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
-                                                __uint_as_float(orr[2 * i + 1]) * inv_l);
-                        // 16-byte chunk c of the row lands at chunk c ^ (row mod 8)
-#pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4)
-                            st_shared_v4(srow + ((((uint32_t)(c2 * 4 + k4)) ^ sw) << 4), pk[4 * k4],
-                                         pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
-                    }
+                    for (int k4 = 0; k4 < 8; ++k4)
+                        st_shared_v4(srow + ((((uint32_t)k4) ^ sw) << 4), pk[hh * 32 + 4 * k4],
+                                     pk[hh * 32 + 4 * k4 + 1], pk[hh * 32 + 4 * k4 + 2],
+                                     pk[hh * 32 + 4 * k4 + 3]);
                     fence_proxy_async_smem();  // generic-proxy writes -> visible to the TMA engine
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(C::STG_FULL + t));
                     if (r_in_tile == 0) {
                         if (wait_bar(bar(C::STG_FULL + t), stg_cnt & 1u, wc, SITE_STG_FULL)) {
-                            tma_store_4d(&tm_o, s_base + C::kStageOff + (uint32_t)t * C::kStageBytes,
-                                         hh * 64, it.h, (p.varlen ? it.q_row0 : 0) + t_m0 / p.pack,
-                                         p.varlen ? 0 : it.b);
+                            tma_store_4d(&tm_o, stile, hh * 64, io.h, (p.varlen ? io.q_row0 : 0) +
+                                         (o_m0 >> p.pack_shift), p.varlen ? 0 : io.b);
                             bulk_commit_group();
-                            bulk_wait_group_read0();
-                            mbar_arrive(bar(C::STG_EMPTY + t));
+                            if (hh + 1 < D / 64) {
+                                bulk_wait_group_read0();
+                                mbar_arrive(bar(C::STG_EMPTY + t));
+                            } else {
+                                stg_owed = true;
+                            }
                         } else {
-                            aborted = true;
+                            bad = true;
                         }
                     }
                     ++stg_cnt;
                 }
-                if (__any_sync(0xffffffffu, aborted)) break;
+                if (__any_sync(0xffffffffu, bad)) {
+                    aborted = true;
+                    break;
+                }
             } else {
 #pragma unroll 1
                 for (int c = 0; c < D; c += 32) {
@@ -1062,14 +1141,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if constexpr (PAIR)
-                    mbar_arrive_cluster(leader(bar(C::O_EMPTY + t)));
-                else
-                    mbar_arrive(bar(C::O_EMPTY + t));
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (PAIR)
+                        mbar_arrive_cluster(leader(bar(C::O_EMPTY + t)));
+                    else
+                        mbar_arrive(bar(C::O_EMPTY + t));
+                }
             }
             if (row_ok)
                 *lse_ptr = has_mass ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;

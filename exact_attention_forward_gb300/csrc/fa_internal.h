@@ -30,6 +30,7 @@ struct FwdParams {
     int kv_group;               // query heads per K/V head (grouped-query attention; 1 = MHA)
     int pack;                   // > 1: the kv_group query heads of a K/V head share tiles
                                 //   (rows = query row x head); 1: one head per tile
+    int pack_shift;             // log2(pack) (pack is a power of two)
     int item_heads;             // heads the items run over: heads, or heads / pack
     int seqlen_q, seqlen_k;     // fixed length: the lengths; varlen: max lengths
     int total_q;                // varlen: packed rows of Q (LSE row stride)
