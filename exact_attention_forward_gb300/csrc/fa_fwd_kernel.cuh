@@ -51,12 +51,13 @@
 //     streams is slower, and so is moving part of exp2 to the FMA pipe -- on
 //     GB300 the MUFU is not the limit;
 //   * the producer decides each CTA's next item (static LPT snake for fixed
-//     length, a device-wide counter for varlen) and hands the index to the other
-//     roles through a two-entry ring in shared memory, before the current item's
-//     epilogue;
-//   * the epilogue normalises O from TMEM into a 128-byte-swizzled staging tile
-//     and writes it out with a TMA store (plain stores only where a varlen tile
-//     crosses its sequence end, and for the fp32 split partials);
+//     length, a device-wide counter for varlen), decodes it once and hands the
+//     decoded record to the other roles through a two-entry ring in shared memory,
+//     before the current item's epilogue;
+//   * the epilogue reads O out of TMEM (normalised, packed to bf16) and returns the
+//     TMEM columns to the MMA issuer at once, then writes O out through a
+//     128-byte-swizzled staging tile with TMA stores (plain stores only where a
+//     varlen tile crosses its sequence end, and for the fp32 split partials);
 //   * every wait is bounded by wall clock; a timeout sets the device error
 //     word and all roles abandon the launch cleanly (TMEM released);
 //   * CTA-pair variant (PAIR, bf16, D = 128): a cluster of two CTAs on two SMs
