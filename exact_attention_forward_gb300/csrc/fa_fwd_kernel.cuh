@@ -1152,7 +1152,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (row_ok)
-                *lse_ptr = has_mass ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+                // (l_run >= 1 for a row with mass: the reference max never exceeds the row max)
+                *lse_ptr = has_mass ? (m_run + lg2_approx(l_run)) * 0.69314718055994531f : -INFINITY;
         }
     }
 
