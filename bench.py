@@ -350,12 +350,20 @@ def run_gpu(args, w):
     if pair and (fp8 or w.head_dim != 128 or w.cache_new):
         raise SystemExit("--cta-pair runs the bf16 head-dim-128 attention workloads only")
     if not w.varlen and not pair:
-        need = fa.workspace_size(w.batch, w.heads, w.seqlen_q, w.seqlen_k, w.head_dim, w.causal,
-                                 heads_k=w.kv_heads)
+        if w.cache_new:
+            need = fa.kvcache_workspace_size(w.batch, w.heads, w.kv_heads, w.seqlen_q, w.seqlen_k,
+                                             w.head_dim, w.causal)
+        else:
+            need = fa.workspace_size(w.batch, w.heads, w.seqlen_q, w.seqlen_k, w.head_dim, w.causal,
+                                     heads_k=w.kv_heads)
         if need:
             ws = torch.empty(need, dtype=torch.uint8, device=dev)
-    splits = (fa.num_splits(w.batch, w.heads, w.seqlen_q, w.seqlen_k, w.causal, heads_k=w.kv_heads)
-              if ws is not None else 1)
+    if ws is None:
+        splits = 1
+    elif w.cache_new:
+        splits = fa.kvcache_num_splits(w.batch, w.heads, w.kv_heads, w.seqlen_q, w.seqlen_k, w.causal)
+    else:
+        splits = fa.num_splits(w.batch, w.heads, w.seqlen_q, w.seqlen_k, w.causal, heads_k=w.kv_heads)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)

@@ -29,6 +29,7 @@ import os
 import threading
 
 __all__ = ["fwd", "fwd_kvcache", "fa_fwd", "FaError", "workspace_size", "num_splits",
+           "kvcache_workspace_size", "kvcache_num_splits",
            "device_error", "debug_set", "library_path", "EXPORTED_SYMBOLS", "load_library"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -42,7 +43,8 @@ FA_DTYPE_BF16, FA_DTYPE_E4M3, FA_DTYPE_E5M2 = 0, 1, 2
 EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_num_splits", "fa_status_string",
                     "fa_last_error_detail", "fa_device_error", "fa_debug_set",
                     "fa_fwd_static_workspace", "fa_fwd_gqa", "fa_fwd_fp8", "fa_fwd_kvcache",
-                    "fa_fwd_workspace_size_gqa", "fa_fwd_num_splits_gqa", "fa_fwd_2cta")
+                    "fa_fwd_workspace_size_gqa", "fa_fwd_num_splits_gqa", "fa_fwd_2cta",
+                    "fa_fwd_kvcache_workspace_size", "fa_fwd_kvcache_num_splits")
 
 _lock = threading.Lock()
 _lib = None
@@ -101,6 +103,10 @@ def load_library():
         lib.fa_fwd_kvcache.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp,
                                        i32, i32, f32, i32, i32, i32, vp, vp, vp, i64, i64, vp, sz,
                                        vp]
+        lib.fa_fwd_kvcache_workspace_size.restype = sz
+        lib.fa_fwd_kvcache_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+        lib.fa_fwd_kvcache_num_splits.restype = i32
+        lib.fa_fwd_kvcache_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.fa_fwd_2cta.restype = i32
         lib.fa_fwd_2cta.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, i32,
                                     i32, f32, i32, vp]
@@ -125,6 +131,17 @@ def workspace_size(batch, heads, seqlen_q, seqlen_k, head_dim_v, causal=False, h
     return int(load_library().fa_fwd_workspace_size_gqa(
         batch, heads, heads if heads_k is None else heads_k, seqlen_q, seqlen_k, head_dim_v,
         int(bool(causal))))
+
+
+def kvcache_workspace_size(batch, heads, heads_k, seqlen_q, cache_capacity, head_dim,
+                           causal=False) -> int:
+    return int(load_library().fa_fwd_kvcache_workspace_size(
+        batch, heads, heads_k, seqlen_q, cache_capacity, head_dim, int(bool(causal))))
+
+
+def kvcache_num_splits(batch, heads, heads_k, seqlen_q, cache_capacity, causal=False) -> int:
+    return int(load_library().fa_fwd_kvcache_num_splits(
+        batch, heads, heads_k, seqlen_q, cache_capacity, int(bool(causal))))
 
 
 def num_splits(batch, heads, seqlen_q, seqlen_k, causal=False, heads_k=None) -> int:
@@ -337,7 +354,7 @@ def fwd_kvcache(q, k_cache, v_cache, cache_seqlens, k_new=None, v_new=None, *, c
         ds, ds_b, ds_h = _fp8_descales(descale, batch, heads_k, dev, temps)
     ws, ws_bytes = None, 0
     if isinstance(workspace, str):
-        need = workspace_size(batch, heads, sq, cap, d, causal, heads_k=heads_k) if sq > 0 else 0
+        need = kvcache_workspace_size(batch, heads, heads_k, sq, cap, d, causal) if sq > 0 else 0
         if need > 0:
             ws = torch.empty(need, dtype=torch.uint8, device=dev)
             ws_bytes = need

@@ -155,6 +155,23 @@ int plan_splits(int batch, int heads, int heads_k, int sq, int sk, int causal, i
     return choose_splits(batch, heads / pack, sq * pack, sk, causal, sms);
 }
 
+// Balanced plan for key/value-cache launches (cache lengths live on the device, so items
+// differ in cost in ways the host cannot see): when the fixed-length rule does not split,
+// the items are few (< 2 waves) and long, every CTA takes an equal share of the key
+// blocks of all items, concatenated -- at most kStreamSlots pieces per item, merged by the
+// LSE identity.  The batch's lengths are read into shared memory by each CTA (<= 64).
+constexpr int kStreamSlots = 4;
+constexpr int kStreamMaxBatch = 64;
+bool use_stream_plan(int batch, int heads, int heads_k, int sq, int cap, int causal, int sms) {
+    const int pack = choose_pack(heads, heads_k, sq, false);
+    const long long mpairs = ceil_div((long long)sq * pack, 256);
+    const long long items = mpairs * batch * (heads / pack);
+    // (rows that see only part of their item's keys -- a causal mask over several query
+    // rows -- would leave pieces without work: not planned this way)
+    return batch <= kStreamMaxBatch && mpairs == 1 && items < 2LL * sms && ceil_div(cap, 128) >= 8 &&
+           (!causal || sq == 1) && plan_splits(batch, heads, heads_k, sq, cap, causal, sms) == 1;
+}
+
 size_t workspace_bytes_for(int splits, int batch, int heads, int sq, int dv) {
     if (splits <= 1) return 0;
     const size_t rows = (size_t)splits * batch * heads * sq;
@@ -243,8 +260,13 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const float* __restrict
                 w = __shfl_sync(0xffffffffu, w_lane, s) * inv;  // 0 past the last split
             else if (s < splits)
                 w = expf(__ldg(ws_lse + s * stride + row) - mx) * inv;
+            // (a slot of weight 0 -- an empty split, or a piece slot the balanced cache plan
+            // did not use -- adds nothing, and its O is not trusted: never written for unused
+            // slots)
+            if (w != 0.f) {
 #pragma unroll
-            for (int c = 0; c < kCols; ++c) acc[c] = fmaf(w, v[u][c], acc[c]);
+                for (int c = 0; c < kCols; ++c) acc[c] = fmaf(w, v[u][c], acc[c]);
+            }
         }
     }
     if constexpr (kCols == 4) {
@@ -373,8 +395,11 @@ fa_status fwd_impl(const FwdArgs& a) {
     // ---------------------------------------------------------------- decomposition
     const int pack = a.cta_pair ? 1 : choose_pack(a.heads, a.heads_k, mq, varlen);
     int splits = 1;
+    const bool stream = a.seqused_k && a.workspace && mq > 0 &&
+                        use_stream_plan(a.batch, a.heads, a.heads_k, a.seqlen_q, a.seqlen_k, a.causal, sms);
     if (!varlen && a.workspace && mq > 0) {
-        splits = plan_splits(a.batch, a.heads, a.heads_k, a.seqlen_q, a.seqlen_k, a.causal, sms);
+        splits = stream ? kStreamSlots
+                        : plan_splits(a.batch, a.heads, a.heads_k, a.seqlen_q, a.seqlen_k, a.causal, sms);
         const size_t need = workspace_bytes_for(splits, a.batch, a.heads, a.seqlen_q, a.head_dim_v);
         if (a.workspace_bytes < need)
             return fail(FA_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed",
@@ -419,6 +444,8 @@ fa_status fwd_impl(const FwdArgs& a) {
     p.varlen = varlen ? 1 : 0;
     p.greedy = varlen && !a.cta_pair ? 1 : 0;  // varlen item costs are unknown on the host
     p.split = splits > 1 ? 1 : 0;
+    p.stream = stream ? 1 : 0;
+    if (stream) p.n_items = 1;  // pieces are published as index 0, the end as index 1
     p.v_e5m2 = a.v_dtype == FA_DTYPE_E5M2 ? 1 : 0;
     if (p.split) {
         const size_t rows = (size_t)splits * a.batch * a.heads * a.seqlen_q;
@@ -473,7 +500,7 @@ fa_status fwd_impl(const FwdArgs& a) {
         if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
         return FA_OK;
     }
-    const int grid = (int)(n_items < sms ? n_items : sms);
+    const int grid = stream ? sms : (int)(n_items < sms ? n_items : sms);
     if (fp8)
         e = launch_fwd_e4m3_d128(tq, tk, tv, to, p, grid, s, append);
     else if (a.head_dim == 64)
@@ -558,6 +585,24 @@ size_t fa_fwd_workspace_size_gqa(int batch, int heads, int heads_k, int seqlen_q
     const int s = fa_fwd_num_splits_gqa(batch, heads, heads_k, seqlen_q, seqlen_k, causal);
     if (head_dim_v < 1) return 0;
     return workspace_bytes_for(s, batch, heads, seqlen_q, head_dim_v);
+}
+
+int fa_fwd_kvcache_num_splits(int batch, int heads, int heads_k, int seqlen_q, int cache_capacity,
+                              int causal) {
+    int dev, sms;
+    uint32_t* err;
+    if (batch < 1 || heads < 1 || seqlen_q < 1 || cache_capacity < 1) return 1;
+    if (heads_k < 1 || heads % heads_k != 0) return 1;
+    if (device_info(&dev, &sms, &err) != FA_OK) return 1;
+    if (use_stream_plan(batch, heads, heads_k, seqlen_q, cache_capacity, causal, sms)) return kStreamSlots;
+    return plan_splits(batch, heads, heads_k, seqlen_q, cache_capacity, causal, sms);
+}
+
+size_t fa_fwd_kvcache_workspace_size(int batch, int heads, int heads_k, int seqlen_q,
+                                     int cache_capacity, int head_dim, int causal) {
+    const int s = fa_fwd_kvcache_num_splits(batch, heads, heads_k, seqlen_q, cache_capacity, causal);
+    if (head_dim < 1) return 0;
+    return workspace_bytes_for(s, batch, heads, seqlen_q, head_dim);
 }
 
 size_t fa_fwd_workspace_size(int batch, int heads, int seqlen_q, int seqlen_k, int head_dim_v,

@@ -147,7 +147,10 @@ struct Cfg {
     // misc: TMEM address, abort flag, item ring indices (16 B); then the two decoded item
     // records of the ring (64 B each, 16-byte aligned)
     static constexpr int kItemRecOff = (kMiscOff + 16 + 15) / 16 * 16;
-    static constexpr int kSmemBytes = kItemRecOff + 2 * 64 + 1024;  // + slack to align the base to 1 KiB
+    // balanced cache plan: the batch's clamped cache lengths (<= 64 sequences), producer only
+    static constexpr int kLenOff = kItemRecOff + 2 * 64;
+    static constexpr int kMaxPlanBatch = 64;
+    static constexpr int kSmemBytes = kLenOff + kMaxPlanBatch * 4 + 1024;  // + slack to align the base to 1 KiB
     static constexpr int kMmaM = PAIR ? 2 * kBM : kBM;  // rows of one MMA (both CTAs of a pair)
     static constexpr uint32_t kIdescQK = make_idesc(kMmaM, kBN, 0u + (FP8 ? 0u : 1u), false);
     static constexpr uint32_t kIdescPV = make_idesc(kMmaM, D, 0u + (FP8 ? 0u : 1u), true);
@@ -172,7 +175,34 @@ struct Item {
     int n_hi_t[kTiles];  // tile t visits [n_lo, n_hi_t[t]); none if n_hi_t[t] <= n_lo
     bool active[kTiles]; // tile t has at least one row inside the sequence
     bool bad_len;        // the per-sequence key length was out of range (clamped)
+    int fill;            // balanced plan: partial slots after this piece's to mark empty
 };
+
+// Tile rows and visited key blocks [n_lo, n_hi_t[t]) of an item whose rows start at
+// (packed) row mp * kTiles * kSlotRows and whose key range is [n_lo, n_end), under the
+// causal mask when set (bottom-right aligned).
+template <bool PAIR>
+__device__ __forceinline__ void set_tile_ranges(const FwdParams& p, Item& it, int mp, int n_end,
+                                                uint32_t rank) {
+    constexpr int kSlotRows = PAIR ? 2 * kBM : kBM;  // query rows of one MMA row slot
+    const int G = p.pack;
+    it.n_hi = it.n_lo;
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t) {
+        const int s0 = mp * (kTiles * kSlotRows) + t * kSlotRows;  // first (packed) row of slot t
+        it.m0[t] = s0 + (PAIR ? (int)rank * kBM : 0);               // ... of this CTA's tile
+        it.active[t] = s0 < it.sq * G;
+        int hi = n_end;
+        if (p.causal) {
+            const int rmax = (min(s0 + kSlotRows, it.sq * G) - 1) / G;  // last query row
+            const int last = rmax + it.sk - it.sq;  // last visible key of the tile's last row
+            hi = last < 0 ? 0 : min(hi, last / kBN + 1);
+        }
+        if (!it.active[t]) hi = it.n_lo;
+        it.n_hi_t[t] = max(hi, it.n_lo);
+        it.n_hi = max(it.n_hi, it.n_hi_t[t]);
+    }
+}
 
 // Longest-processing-time order: item index -> pair index descending (under a
 // causal mask later pairs see more key blocks), then (batch, head, split).  Query
@@ -180,8 +210,8 @@ struct Item {
 // they stream the same K/V at about the same time and share it in L2.
 template <bool PAIR>
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int w, uint32_t rank) {
-    constexpr int kSlotRows = PAIR ? 2 * kBM : kBM;  // query rows of one MMA row slot
     Item it;
+    it.fill = 0;
     // packed grouped-query mode (p.pack = G > 1): an item serves one K/V head, and its
     // tile rows are (query row, query head of the group) pairs, row-major: packed row
     // r = i * G + g.  it.h is then the group's first query head.
@@ -212,23 +242,7 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int w, uint32_t 
     }
     const int nblk = (it.sk + kBN - 1) / kBN;
     it.n_lo = it.split * p.blocks_per_split;
-    const int n_end = min(nblk, it.n_lo + p.blocks_per_split);
-    it.n_hi = it.n_lo;
-#pragma unroll
-    for (int t = 0; t < kTiles; ++t) {
-        const int s0 = mp * (kTiles * kSlotRows) + t * kSlotRows;  // first (packed) row of slot t
-        it.m0[t] = s0 + (PAIR ? (int)rank * kBM : 0);               // ... of this CTA's tile
-        it.active[t] = s0 < it.sq * G;
-        int hi = n_end;
-        if (p.causal) {
-            const int rmax = (min(s0 + kSlotRows, it.sq * G) - 1) / G;  // last query row
-            const int last = rmax + it.sk - it.sq;  // last visible key of the tile's last row
-            hi = last < 0 ? 0 : min(hi, last / kBN + 1);
-        }
-        if (!it.active[t]) hi = it.n_lo;
-        it.n_hi_t[t] = max(hi, it.n_lo);
-        it.n_hi = max(it.n_hi, it.n_hi_t[t]);
-    }
+    set_tile_ranges<PAIR>(p, it, mp, min(nblk, it.n_lo + p.blocks_per_split), rank);
     return it;
 }
 
@@ -240,7 +254,7 @@ __device__ __forceinline__ void store_item(uint8_t* rec, int w, const Item& it) 
     r[0] = make_int4(w, it.b, it.h, it.split);
     r[1] = make_int4(it.sq, it.sk, it.q_row0, it.k_row0);
     r[2] = make_int4(it.m0[0], it.m0[1], it.n_lo, it.n_hi);
-    r[3] = make_int4(it.n_hi_t[0], it.n_hi_t[1], flags, 0);
+    r[3] = make_int4(it.n_hi_t[0], it.n_hi_t[1], flags, it.fill);
 }
 __device__ __forceinline__ int load_item(const uint8_t* rec, Item& it) {
     const int4* r = reinterpret_cast<const int4*>(rec);
@@ -250,6 +264,7 @@ __device__ __forceinline__ int load_item(const uint8_t* rec, Item& it) {
     it.m0[0] = c.x; it.m0[1] = c.y; it.n_lo = c.z; it.n_hi = c.w;
     it.n_hi_t[0] = d.x; it.n_hi_t[1] = d.y;
     it.active[0] = (d.z & 1) != 0; it.active[1] = (d.z & 2) != 0; it.bad_len = (d.z & 4) != 0;
+    it.fill = d.w;
     return a.x;
 }
 
@@ -421,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // decodes item w (an index below p.n_items) into `it` and publishes both
             auto publish = [&](int w, Item& it) -> bool {
                 const uint32_t slot = published & 1u;
-                if (w < p.n_items) it = decode_item<PAIR>(p, w, rank);
+                if (!p.stream && w < p.n_items) it = decode_item<PAIR>(p, w, rank);
                 if (published >= 2 &&
                     !wait_bar(bar(C::ITEM_EMPTY + slot), ((published >> 1) - 1) & 1u, wc, SITE_ITEM_EMPTY))
                     return false;
@@ -444,9 +459,92 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // a pair's two producers follow one static order (no device counter)
             const bool greedy = !PAIR && p.greedy;
+            // Balanced cache plan (p.stream): the key blocks of all items, concatenated in
+            // (batch, item head) order, are cut into equal shares of T blocks, one per CTA:
+            // this CTA runs the pieces of the items that overlap [lo_g, hi_g), each in its own
+            // partial slot (the CTA index minus that of the item's first share), and finishes
+            // the empty items whose position falls in its share (the last CTA any beyond).
+            // T is at least a third of a full cache, so no item needs more than four slots.
+            // (The plan is used where every row sees every key of its item -- non-causal, or
+            // one query row -- so a piece always has work for its active tiles.)
+            uint32_t* const plan_len = reinterpret_cast<uint32_t*>(smem + C::kLenOff);
+            long long plan_T = 1, lo_g = 0, hi_g = 0, ppos = 0;
+            int pb = 0, ph = 0;  // next item (batch, item head) of the walk, at block ppos
+            if (p.stream) {
+                long long W = 0;
+                for (int b = 0; b < p.batch; ++b) {
+                    const int u = __ldg(p.seqused_k + b) + p.seqused_add;
+                    const int L = min(max(u, 0), p.seqlen_k);
+                    plan_len[b] = (uint32_t)L | ((u < 0 || u > p.seqlen_k) ? 0x80000000u : 0u);
+                    W += (long long)((L + kBN - 1) / kBN) * p.item_heads;
+                }
+                const long long G = gridDim.x;
+                const long long capblk = (p.seqlen_k + kBN - 1) / kBN;
+                plan_T = max(max((W + G - 1) / G, (capblk + p.n_splits - 2) / (p.n_splits - 1)), 1LL);
+                lo_g = (long long)blockIdx.x * plan_T;
+                hi_g = min(lo_g + plan_T, W);
+            }
+            auto next_piece = [&](Item& it) -> bool {
+                const long long G = gridDim.x, c = blockIdx.x, T = plan_T;
+                while (pb < p.batch) {
+                    const uint32_t rec = plan_len[pb];
+                    const int L = (int)(rec & 0x7fffffffu);
+                    const long long nb = (L + kBN - 1) / kBN;
+                    if (ph == 0) {
+                        // nothing from here on is this CTA's (the last CTA also owns any
+                        // empty items beyond the total)
+                        if (ppos >= (c + 1) * T && c != G - 1) return false;
+                        // the whole sequence lies before this CTA's share, or is empty and
+                        // owned by another CTA
+                        if ((nb > 0 && ppos + nb * p.item_heads <= lo_g) ||
+                            (nb == 0 && min(ppos / T, G - 1) != c)) {
+                            ppos += nb * p.item_heads;
+                            ++pb;
+                            continue;
+                        }
+                    }
+                    const int b = pb, h = ph;
+                    const long long s0 = ppos;
+                    ppos += nb;
+                    if (++ph == p.item_heads) {
+                        ph = 0;
+                        ++pb;
+                    }
+                    if (nb == 0) {
+                        // an empty cache (this CTA's to finish): every partial slot of the
+                        // item's rows is marked empty, and the merge writes O = 0, LSE = -inf
+                        const size_t slot_rows = (size_t)p.batch * p.heads * p.seqlen_q;
+                        for (int prow = 0; prow < (p.seqlen_q << p.pack_shift); ++prow) {
+                            const int hrow = h * p.pack + (prow & (p.pack - 1));
+                            const size_t rid = ((size_t)b * p.heads + hrow) * p.seqlen_q + (prow >> p.pack_shift);
+                            for (int k = 0; k < p.n_splits; ++k) p.ws_lse[k * slot_rows + rid] = -INFINITY;
+                        }
+                        continue;
+                    }
+                    const long long a = max(s0, lo_g), e = min(s0 + nb, hi_g);
+                    if (a >= e) continue;  // this item does not reach into the share
+                    const int n_lo = (int)(a - s0), n_end = (int)(e - s0);
+                    const int slot = (int)(c - s0 / T);
+                    const int fill = (e == s0 + nb) ? p.n_splits - 1 - slot : 0;  // the item's last piece
+                    it.b = b;
+                    it.h = h * p.pack;
+                    it.split = slot;
+                    it.fill = fill;
+                    it.q_row0 = b * p.seqlen_q;
+                    it.sq = p.seqlen_q;
+                    it.k_row0 = b * p.seqlen_k;
+                    it.sk = L;
+                    it.bad_len = (rec >> 31) != 0u;
+                    it.n_lo = n_lo;
+                    set_tile_ranges<PAIR>(p, it, 0, n_end, rank);
+                    return true;
+                }
+                return false;
+            };
             int w_next = unit;
             int round_no = 0;  // static order: rounds of the snake
             Item it_next{};
+            if (p.stream) w_next = next_piece(it_next) ? 0 : 1;  // (index 1 = p.n_items: the end)
             if (!publish(w_next, it_next)) aborted = true;
             for (int w = w_next; !aborted && w < p.n_items; w = w_next) {
                 // the next index is requested now and published once this item's loads have
@@ -549,7 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (aborted) break;
-                if (greedy) {
+                if (p.stream) {
+                    w_next = next_piece(it_next) ? 0 : 1;
+                } else if (greedy) {
                     w_next = min((int)(gridDim.x + ticket), p.n_items);
                     if (w_next >= p.n_items) fetching_done();
                 } else {
@@ -798,6 +898,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 o_ptr = reinterpret_cast<__nv_bfloat16*>(p.o) + (((size_t)b * p.seqlen_q + row) * p.heads + hrow) * D;
             }
             return prow < (sq << p.pack_shift);
+        };
+        // balanced cache plan: an item's last piece marks the item's later partial slots of
+        // this row empty (LSE = -inf; the merge gives such slots weight 0 and never reads
+        // their O), so the merge sees exactly the item's pieces (at most 3 later slots)
+        auto mark_empty_slots = [&](float* lse_ptr, int fill) {
+            const size_t slot_rows = (size_t)p.batch * p.heads * p.seqlen_q;
+#pragma unroll
+            for (int k2 = 1; k2 <= 3; ++k2)
+                if (k2 <= fill) lse_ptr[k2 * slot_rows] = -INFINITY;
         };
         for (;;) {
             int w = 0;
@@ -1151,9 +1260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive(bar(C::O_EMPTY + t));
                 }
             }
-            if (row_ok)
+            if (row_ok) {
                 // (l_run >= 1 for a row with mass: the reference max never exceeds the row max)
                 *lse_ptr = has_mass ? (m_run + lg2_approx(l_run)) * 0.69314718055994531f : -INFINITY;
+                if (p.split) mark_empty_slots(lse_ptr, io.fill);
+            }
         }
     }
 

@@ -42,6 +42,8 @@ struct FwdParams {
     float scale_log2;           // softmax_scale * log2(e)
     int causal, varlen, split;
     int greedy;                 // items handed out by the device counter (varlen) or a static snake
+    int stream;                 // cache launches: balanced plan -- each CTA takes an equal share
+                                //   of all items' key blocks (pieces in n_splits partial slots)
     int v_e5m2;                 // FP8: V stored as E5M2 (Q, K and P stay E4M3)
     uint64_t wait_limit_ns;     // bound of every device-side wait
     uint32_t inject;            // debug fault injection (see fa_debug_set)

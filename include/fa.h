@@ -203,10 +203,9 @@ FA_API fa_status fa_fwd_2cta(const void* q, const void* k, const void* v,
  * cache_seqlens lives on the device, so it is checked there: a sequence with
  * cache_seqlens[b] < 0 or cache_seqlens[b] + seqlen_new > cache_capacity gets no
  * rows appended, its attention uses the length clamped to [0, capacity], and
- * fa_device_error() afterwards returns FA_ERR_DEVICE_ARG.  workspace: as fa_fwd
- * (key splits for short-query / long-cache shapes, sized by
- * fa_fwd_workspace_size_gqa(batch, heads, heads_k, seqlen_q, cache_capacity,
- * head_dim, causal)).
+ * fa_device_error() afterwards returns FA_ERR_DEVICE_ARG.  workspace: partial
+ * results of key splits, sized by fa_fwd_kvcache_workspace_size below; NULL means
+ * one CTA per work item.
  */
 FA_API fa_status fa_fwd_kvcache(const void* q, void* k_cache, void* v_cache,
                                 const void* k_new, const void* v_new,
@@ -246,6 +245,21 @@ FA_API size_t fa_fwd_workspace_size_gqa(int batch, int heads, int heads_k, int s
                                         int seqlen_k, int head_dim_v, int causal);
 FA_API int fa_fwd_num_splits_gqa(int batch, int heads, int heads_k, int seqlen_q, int seqlen_k,
                                  int causal);
+
+/*
+ * The same two queries for fa_fwd_kvcache.  Cache lengths differ per sequence and are
+ * known only on the device.  Where the fixed-length rule would not split and the work
+ * items are few (under two waves), long (>= 8 key blocks of capacity) and see all
+ * their keys (non-causal, or one query row), with batch <= 64, a cache call is
+ * balanced instead: every CTA takes an equal share of the key blocks of all items,
+ * computed on the device from cache_seqlens, and each item's pieces (at most 4) are
+ * merged by the LSE identity.  These queries return that plan's needs; a smaller
+ * workspace gives FA_ERR_WORKSPACE, none gives one CTA per item.
+ */
+FA_API size_t fa_fwd_kvcache_workspace_size(int batch, int heads, int heads_k, int seqlen_q,
+                                            int cache_capacity, int head_dim, int causal);
+FA_API int fa_fwd_kvcache_num_splits(int batch, int heads, int heads_k, int seqlen_q,
+                                     int cache_capacity, int causal);
 
 /*
  * fa_fwd_static_workspace -- fa_fwd for fixed-length inputs, for callers that

@@ -158,9 +158,12 @@ def test_kvcache_append_and_attend(B, H, Hk, Sq, cap, lens, n_new, causal):
 
 
 def test_kvcache_decode_many_items():
-    # 16 sequences x 8 K/V heads = 128 packed decode items (one per CTA, no key splits);
-    # lengths include empty, one row, a full cache, block edges and random ones
+    # 16 sequences x 8 K/V heads = 128 packed decode items, fewer than two waves: the
+    # balanced plan (equal shares of all items' key blocks, pieces merged); lengths include
+    # empty, one row, a full cache, block edges and random ones
     B, H, Hk, Sq, cap, n_new = 16, 32, 8, 1, 2048, 1
+    assert fa.kvcache_num_splits(B, H, Hk, Sq, cap, True) == 4
+    assert fa.kvcache_workspace_size(B, H, Hk, Sq, cap, 128, True) > 0
     rng = np.random.default_rng(350)
     lens = [0, 1, cap - 1, 127, 128, 129] + [int(v) for v in rng.integers(0, cap, size=B - 6)]
     xc, new, lens_t = _cache_case(B, H, Hk, Sq, cap, lens, n_new, seed=350)
@@ -173,6 +176,30 @@ def test_kvcache_decode_many_items():
                                       causal=True, seqused_k=[l + n_new for l in lens])
     compare(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
             o_ref, lse_ref, what="kvcache decode, 128 items")
+
+
+@pytest.mark.parametrize("B,H,Hk,Sq,cap,n_new,dtype,v_dtype", [
+    (24, 16, 4, 8, 1500, 8, "bf16", ""),      # packed 4 heads x 8 rows, non-causal
+    (20, 8, 4, 1, 3000, 1, "e4m3", "e5m2"),   # FP8 cache with E5M2 V, per-head descales
+    (64, 4, 4, 1, 1100, 1, "bf16", ""),       # the largest planned batch, MHA decode
+])
+def test_kvcache_balanced_plan(B, H, Hk, Sq, cap, n_new, dtype, v_dtype):
+    causal = Sq == 1
+    assert fa.kvcache_num_splits(B, H, Hk, Sq, cap, causal) == 4
+    rng = np.random.default_rng(360 + B)
+    lens = [0, cap - n_new] + [int(v) for v in rng.integers(0, cap - n_new + 1, size=B - 2)]
+    xc, new, lens_t = _cache_case(B, H, Hk, Sq, cap, lens, n_new, seed=360 + B, dtype=dtype,
+                                  v_dtype=v_dtype)
+    o, lse, kc, vc = _run_cache(xc, new, lens_t, causal)
+    st, flags = fa.device_error(clear=True)
+    assert st == fa.FA_OK, f"device error word {flags:#x}"
+    k_ref = oracle.append_kv(xc["k"], new[0], lens)
+    v_ref = oracle.append_kv(xc["v"], new[1], lens)
+    extra = {"descale": xc["descale"]} if dtype == "e4m3" else {}
+    o_ref, lse_ref = oracle.attention(xc["q"], k_ref, v_ref, softmax_scale=128 ** -0.5,
+                                      causal=causal, seqused_k=[l + n_new for l in lens], **extra)
+    compare(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+            o_ref, lse_ref, dtype=dtype, what=f"kvcache balanced plan {(B, H, Hk, Sq, cap)}")
 
 
 def test_kvcache_fp8_head_descales_e5m2_v():
