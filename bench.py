@@ -526,7 +526,11 @@ def run_gpu(args, w):
         "config": dict(_config(w, "flushed between timed steps (256 MiB write + 256 MiB read, untimed)"),
                        kernel="cta_pair (clusters of 2, cta_group::2)" if pair else "one CTA per SM"),
         "clocks": clocks, "e2e": e2e,
-        "gpu_launches": args.steps * ((2 if splits > 1 else 1) + (1 if cache is not None else 0)),
+        # per step: the forward kernel, the split merge when the key range is split, and the
+        # cache-append copy kernel when a call appends more than 4 rows per sequence (fewer
+        # are written by the forward kernel itself)
+        "gpu_launches": args.steps * ((2 if splits > 1 else 1) +
+                                      (1 if cache is not None and w.cache_new > 4 else 0)),
         "roofline": roofline,
         "step_ms": {"min": min(times_ms), "median": statistics.median(times_ms),
                     "max": max(times_ms)},

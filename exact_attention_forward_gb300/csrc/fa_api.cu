@@ -485,7 +485,18 @@ fa_status fwd_impl(const FwdArgs& a) {
     // ---------------------------------------------------------------- launches
     cudaStream_t s = static_cast<cudaStream_t>(a.stream);
     cudaError_t e;
-    if (append) {  // the new rows go into the cache first (same stream: ordered before the reads)
+    // Few new rows (decoding): written by the forward kernel's producers, each the rows in
+    // the key blocks it loads, right before loading them -- no copy kernel.  Otherwise a
+    // copy kernel runs first on the same stream.
+    const bool fused_append = append && rows_q > 0 && mq > 0 && a.n_new <= 4;
+    if (fused_append) {
+        p.k_cache = const_cast<void*>(a.k);
+        p.v_cache = const_cast<void*>(a.v);
+        p.k_new = a.k_new;
+        p.v_new = a.v_new;
+        p.append_rows = a.n_new;
+    }
+    if (append && !fused_append) {  // the new rows go into the cache first (ordered before the reads)
         const long long row_bytes = (long long)a.heads_k * a.head_dim * (fp8 ? 1 : 2);
         e = launch_append_kv(const_cast<void*>(a.k), const_cast<void*>(a.v), a.k_new, a.v_new,
                              a.seqused_k, a.batch, a.seqlen_k, a.n_new, row_bytes, err, s);
@@ -502,11 +513,11 @@ fa_status fwd_impl(const FwdArgs& a) {
     }
     const int grid = stream ? sms : (int)(n_items < sms ? n_items : sms);
     if (fp8)
-        e = launch_fwd_e4m3_d128(tq, tk, tv, to, p, grid, s, append);
+        e = launch_fwd_e4m3_d128(tq, tk, tv, to, p, grid, s, append && !fused_append);
     else if (a.head_dim == 64)
-        e = launch_fwd_bf16_d64(tq, tk, tv, to, p, grid, s, append);
+        e = launch_fwd_bf16_d64(tq, tk, tv, to, p, grid, s, append && !fused_append);
     else
-        e = launch_fwd_bf16_d128(tq, tk, tv, to, p, grid, s, append);
+        e = launch_fwd_bf16_d128(tq, tk, tv, to, p, grid, s, append && !fused_append);
     if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
     if (p.split) {
         e = launch_combine(p.ws_o, p.ws_lse, a.o, a.lse, a.batch, a.heads, a.seqlen_q,

@@ -623,6 +623,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 auto expect_group = [&](uint32_t full, uint32_t n) {
                     if (rank == 0u) mbar_arrive_expect_tx(full, n * (PAIR ? 2u : 1u) * C::kSlotBytes);
                 };
+                // Few new cache rows (decoding): the ones inside this item's key blocks go
+                // into the caches now, before any of those blocks is loaded -- generic-proxy
+                // writes, a proxy fence, then the TMA reads.  Every new row lies in one block,
+                // and every item that reads that block writes the row itself (items of other
+                // query heads of the same K/V head write the same bytes).  A sequence whose
+                // filled length leaves no room gets no rows; the error word records it.
+                if (!PAIR && p.append_rows > 0 && has_work) {  // (pairs take no cache calls)
+                    const int len = __ldg(p.seqused_k + it.b);
+                    if (len < 0 || len > p.seqlen_k - p.append_rows) {
+                        atomicOr(p.err, kErrBadLength);
+                    } else {
+                        constexpr int kVecs = D * C::kElem / 16;  // 16-byte vectors in one head's row
+                        const int hk = p.heads / p.kv_group;
+                        const int r0 = max(len, it.n_lo * kBN);
+                        const int r1 = min(len + p.append_rows, it.n_hi * kBN);
+                        const uint4* kn = static_cast<const uint4*>(p.k_new);
+                        const uint4* vn = static_cast<const uint4*>(p.v_new);
+                        uint4* kc = static_cast<uint4*>(p.k_cache);
+                        uint4* vc = static_cast<uint4*>(p.v_cache);
+                        for (int r = r0; r < r1; ++r) {
+                            const size_t src = (((size_t)it.b * p.append_rows + (r - len)) * hk + kv_head) * kVecs;
+                            const size_t dst = (((size_t)it.b * p.seqlen_k + r) * hk + kv_head) * kVecs;
+                            for (int c = 0; c < kVecs; ++c) {
+                                kc[dst + c] = __ldg(kn + src + c);
+                                vc[dst + c] = __ldg(vn + src + c);
+                            }
+                        }
+                        fence_proxy_async_global();
+                    }
+                }
                 if (has_work) {
                     const int j0 = it.n_hi - 1;
                     if (!free_slot(ring)) {

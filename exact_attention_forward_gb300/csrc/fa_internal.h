@@ -22,6 +22,11 @@ struct FwdParams {
     const int32_t* seqused_k;   // fixed length: keys of sequence b = seqused_k[b] + seqused_add
     int seqused_add;            //   (nullptr: seqlen_k); lengths outside [0, seqlen_k] are clamped
                                 //   and flagged in the device error word
+    void* k_cache;              // key/value cache calls with few new rows: the producers write
+    void* v_cache;              //   k_new / v_new ([B, append_rows, Hk, D]) into the caches at
+    const void* k_new;          //   the filled length, each the rows inside the key blocks it
+    const void* v_new;          //   loads, just before loading them (0 rows: none here)
+    int append_rows;
     float* ws_o;                // split mode: normalised partial O [splits, B, H, Sq, Dv] fp32
     float* ws_lse;              // split mode: partial LSE [splits, B, H, Sq] fp32
     uint32_t* err;              // device error word

@@ -202,6 +202,48 @@ def test_kvcache_balanced_plan(B, H, Hk, Sq, cap, n_new, dtype, v_dtype):
             o_ref, lse_ref, dtype=dtype, what=f"kvcache balanced plan {(B, H, Hk, Sq, cap)}")
 
 
+@pytest.mark.parametrize("B,H,Hk,Sq,cap,lens,n_new", [
+    (3, 6, 2, 1, 700, [126, 0, 300], 3),   # rows 126-128 cross a key block; group 3 unpacked
+    (2, 8, 2, 2, 1000, [254, 500], 4),     # rows 254-257 cross a block; packed 4 heads x 2 rows
+    (4, 8, 8, 1, 9000, [8999, 0, 5000, 128], 1),  # one new row, cache full after the append
+])
+def test_kvcache_few_new_rows_written_by_the_attention(B, H, Hk, Sq, cap, lens, n_new):
+    # up to 4 new rows per sequence are written by the attention kernel's producers (the
+    # rows inside each item's key blocks, before those blocks are loaded): no copy kernel
+    xc, new, lens_t = _cache_case(B, H, Hk, Sq, cap, lens, n_new, seed=370 + cap)
+    o, lse, kc, vc = _run_cache(xc, new, lens_t, True)
+    st, flags = fa.device_error(clear=True)
+    assert st == fa.FA_OK, f"device error word {flags:#x}"
+    k_ref = oracle.append_kv(xc["k"], new[0], lens)
+    v_ref = oracle.append_kv(xc["v"], new[1], lens)
+    assert torch.equal(kc.cpu().view(torch.int16), k_ref.view(torch.int16))
+    assert torch.equal(vc.cpu().view(torch.int16), v_ref.view(torch.int16))
+    o_ref, lse_ref = oracle.attention(xc["q"], k_ref, v_ref, softmax_scale=128 ** -0.5,
+                                      causal=True, seqused_k=[l + n_new for l in lens])
+    compare(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+            o_ref, lse_ref, what=f"kvcache fused append {(B, H, Hk, Sq, cap, lens, n_new)}")
+
+
+def test_kvcache_fused_append_out_of_range_length():
+    B, H, Hk, Sq, cap, n_new = 2, 4, 2, 1, 300, 1
+    lens = [300, 10]  # 300 + 1 > 300: sequence 0 gets no row, its length is clamped to 300
+    xc, new, lens_t = _cache_case(B, H, Hk, Sq, cap, lens, n_new, seed=380)
+    fa.device_error(clear=True)
+    o, lse, kc, vc = _run_cache(xc, new, lens_t, True)
+    st, flags = fa.device_error(clear=True)
+    assert st == fa.FA_ERR_DEVICE_ARG and flags & 2
+    k_ref = xc["k"].clone()
+    v_ref = xc["v"].clone()
+    k_ref[1, 10:11] = new[0][1]
+    v_ref[1, 10:11] = new[1][1]
+    assert torch.equal(kc.cpu().view(torch.int16), k_ref.view(torch.int16))
+    assert torch.equal(vc.cpu().view(torch.int16), v_ref.view(torch.int16))
+    o_ref, lse_ref = oracle.attention(xc["q"], k_ref, v_ref, softmax_scale=128 ** -0.5,
+                                      causal=True, seqused_k=[300, 11])
+    compare(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+            o_ref, lse_ref, what="kvcache fused append, clamped length")
+
+
 def test_kvcache_fp8_head_descales_e5m2_v():
     B, H, Hk, Sq, cap, lens, n_new = 2, 8, 2, 64, 3000, [1000, 2500], 64
     xc, new, lens_t = _cache_case(B, H, Hk, Sq, cap, lens, n_new, seed=333, dtype="e4m3",
