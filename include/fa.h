@@ -185,9 +185,10 @@ FA_API fa_status fa_fwd_2cta(const void* q, const void* k, const void* v,
  * fa_fwd_kvcache -- append new key/value rows to a key/value cache, then attend
  * over the cache.  The AppendKV branch of the producer loop on the page
  * "FlashAttention core algorithm: forward pass" (scheduler-loop excerpt) loads
- * the new K/V before the attention of the same work tile; here the rows are
- * first written into the cache by a copy kernel, then the forward kernel runs,
- * both on `stream`.
+ * the new K/V before the attention of the same work tile; here, for up to 4 new
+ * rows per sequence, the attention kernel writes them into the cache itself (each
+ * work tile the rows inside the key blocks it loads, before loading them); for
+ * more, a copy kernel writes them first.  Both run on `stream`.
  *   q        [batch, seqlen_q, heads, head_dim]
  *   k_cache, v_cache [batch, cache_capacity, heads_k, head_dim]   (written)
  *   k_new, v_new     [batch, seqlen_new, heads_k, head_dim] or NULL (seqlen_new 0)
