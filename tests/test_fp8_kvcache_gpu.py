@@ -202,6 +202,51 @@ def test_kvcache_balanced_plan(B, H, Hk, Sq, cap, n_new, dtype, v_dtype):
             o_ref, lse_ref, dtype=dtype, what=f"kvcache balanced plan {(B, H, Hk, Sq, cap)}")
 
 
+def test_kvcache_plan_empty_items():
+    # attention only (no new rows) over caches of which some are empty: those items have
+    # no key block, so the CTA whose share holds their position marks every partial slot
+    # of their rows empty, and the merge writes O = 0, LSE = -inf
+    B, H, Hk, Sq, cap = 16, 32, 8, 1, 2048
+    assert fa.kvcache_num_splits(B, H, Hk, Sq, cap, True) == 4
+    lens = [0, 0, cap, 1, 0, 700, 1300, 0, 128, 0, 129, 2000, 0, 5, 1024, 0]
+    xc, _, lens_t = _cache_case(B, H, Hk, Sq, cap, lens, 0, seed=390)
+    o, lse, _, _ = _run_cache(xc, None, lens_t, True)
+    st, flags = fa.device_error(clear=True)
+    assert st == fa.FA_OK, f"device error word {flags:#x}"
+    o_ref, lse_ref = oracle.attention(xc["q"], xc["k"], xc["v"], softmax_scale=128 ** -0.5,
+                                      causal=True, seqused_k=lens)
+    compare(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+            o_ref, lse_ref, what="kvcache balanced plan, empty caches")
+
+
+def test_kvcache_plan_repeated_launches():
+    # Lengths change every launch while the workspace is reused: an item's pieces fall in
+    # other slots each time, so partial rows left by an earlier launch in the slots an item
+    # does not use this time must be marked empty, not merged.  300 launches also wrap the
+    # library's 256 per-launch counter slots.
+    B, H, Hk, Sq, cap = 16, 32, 8, 1, 2048
+    assert fa.kvcache_num_splits(B, H, Hk, Sq, cap, True) == 4
+    xc, _, _ = _cache_case(B, H, Hk, Sq, cap, [cap] * B, 0, seed=395)
+    dev = "cuda"
+    q, kc, vc = xc["q"].to(dev), xc["k"].to(dev), xc["v"].to(dev)
+    rng = np.random.default_rng(395)
+    all_lens = rng.integers(1, cap + 1, size=(300, B)).astype(np.int32)
+    lens_d = torch.from_numpy(all_lens).to(dev)
+    outs = {}
+    for i in range(300):
+        o, lse = fa.fwd_kvcache(q, kc, vc, lens_d[i], causal=True)
+        if i % 60 == 59:
+            outs[i] = (o.float().cpu(), lse.cpu())
+    torch.cuda.synchronize()
+    st, flags = fa.device_error(clear=True)
+    assert st == fa.FA_OK, f"device error word {flags:#x}"
+    for i, (o, lse) in outs.items():
+        o_ref, lse_ref = oracle.attention(xc["q"], xc["k"], xc["v"], softmax_scale=128 ** -0.5,
+                                          causal=True, seqused_k=[int(v) for v in all_lens[i]])
+        compare(o.numpy().astype(np.float64), lse.numpy().astype(np.float64), o_ref, lse_ref,
+                what=f"kvcache balanced plan, launch {i}")
+
+
 @pytest.mark.parametrize("B,H,Hk,Sq,cap,lens,n_new", [
     (3, 6, 2, 1, 700, [126, 0, 300], 3),   # rows 126-128 cross a key block; group 3 unpacked
     (2, 8, 2, 2, 1000, [254, 500], 4),     # rows 254-257 cross a block; packed 4 heads x 2 rows
