@@ -54,6 +54,14 @@
 //     length, a device-wide counter for varlen), decodes it once and hands the
 //     decoded record to the other roles through a two-entry ring in shared memory,
 //     before the current item's epilogue;
+//   * key/value-cache launches with few, long items (decoding) use a balanced
+//     plan instead: every producer reads the cache lengths, and each CTA takes
+//     an equal share of the key blocks of all items, concatenated, as pieces
+//     that leave partial results in their own slots (merged by the LSE identity
+//     in a second, programmatically dependent kernel);
+//   * up to 4 new cache rows per sequence are written into the caches by the
+//     producers themselves (each the rows inside a key block it loads, just
+//     before loading it), so a decoding step needs no copy kernel;
 //   * the epilogue reads O out of TMEM (normalised, packed to bf16) and returns the
 //     TMEM columns to the MMA issuer at once, then writes O out through a
 //     128-byte-swizzled staging tile with TMA stores (plain stores only where a
