@@ -172,6 +172,38 @@ bool use_stream_plan(int batch, int heads, int heads_k, int sq, int cap, int cau
            (!causal || sq == 1) && plan_splits(batch, heads, heads_k, sq, cap, causal, sms) == 1;
 }
 
+// L2-aware order for static schedules.  Taken level by level (all (batch, head) pairs of
+// one pair index, then the next), the ~2 rounds of items running at one time span every
+// (batch, head): at B=2, H=32, S=8192 that is 64 K/V streams of 4 MiB, twice what L2
+// holds, and each K/V block came from DRAM about once per round (reads 4.8x the Q/K/V
+// bytes).  Bands of consecutive levels per (batch, head) put a few heads' items side by
+// side instead.  Item costs: equal without a causal mask, so all levels form one band
+// (head-major).  Under a causal mask the cost falls with the level, and the snake
+// balances it by giving each CTA complementary costs in paired rounds (positions c and
+// 2P-1-c of a run of 2P items, P = CTAs).  A band of g levels keeps that pairing when g
+// divides 2P and a band's items (g x items per level) are a multiple of 2P: g =
+// 2P / gcd(items per level, 2P).  The last ~35 % of the levels (small items, the end of
+// the schedule) stay in plain LPT order.
+void set_item_bands(FwdParams& p, int nunits) {
+    p.band_levels = p.band_items = p.band_lv = 0;
+    if (p.greedy || p.stream || p.varlen || p.seqused_k || p.n_splits != 1 || nunits < 1 ||
+        p.n_items <= nunits)
+        return;
+    const long long per_m = (long long)p.batch * p.item_heads;
+    long long g = p.n_mpairs, bands = 1;
+    if (p.causal) {
+        long long a = per_m, b = 2LL * nunits;
+        while (b) { const long long t = a % b; a = b; b = t; }
+        g = 2LL * nunits / a;
+        const long long tail = (p.n_mpairs * 35LL + 99) / 100;
+        bands = g > 1 ? (p.n_mpairs - tail) / g : 0;
+    }
+    if (bands < 1 || g < 2) return;
+    p.band_levels = (int)g;
+    p.band_lv = (int)(bands * g);
+    p.band_items = (int)(bands * g * per_m);
+}
+
 size_t workspace_bytes_for(int splits, int batch, int heads, int sq, int dv) {
     if (splits <= 1) return 0;
     const size_t rows = (size_t)splits * batch * heads * sq;
@@ -507,11 +539,13 @@ fa_status fwd_impl(const FwdArgs& a) {
         int pairs = 0;
         if ((st = resident_pairs(dev, &pairs)) != FA_OK) return st;
         const int grid2 = 2 * (int)(n_items < pairs ? n_items : pairs);
+        set_item_bands(p, grid2 / 2);
         e = launch_fwd_pair_bf16_d128(tq, tk, tv, to, p, grid2, s);
         if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
         return FA_OK;
     }
     const int grid = stream ? sms : (int)(n_items < sms ? n_items : sms);
+    set_item_bands(p, grid);
     if (fp8)
         e = launch_fwd_e4m3_d128(tq, tk, tv, to, p, grid, s, append && !fused_append);
     else if (a.head_dim == 64)

@@ -54,6 +54,10 @@
 //     length, a device-wide counter for varlen), decodes it once and hands the
 //     decoded record to the other roles through a two-entry ring in shared memory,
 //     before the current item's epilogue;
+//   * static schedules run their items in L2 bands: several consecutive query
+//     tile pairs of one (batch, head) side by side (all of them without a causal
+//     mask; a band sized to keep the snake balanced, then plain LPT, under one),
+//     so the CTAs running at one time read few heads' K/V and find it in L2;
 //   * key/value-cache launches with few, long items (decoding) use a balanced
 //     plan instead: every producer reads the cache lengths, and each CTA takes
 //     an equal share of the key blocks of all items, concatenated, as pieces
@@ -212,10 +216,16 @@ __device__ __forceinline__ void set_tile_ranges(const FwdParams& p, Item& it, in
     }
 }
 
-// Longest-processing-time order: item index -> pair index descending (under a
-// causal mask later pairs see more key blocks), then (batch, head, split).  Query
-// heads sharing a K/V head (grouped-query attention) are consecutive items, so
-// they stream the same K/V at about the same time and share it in L2.
+// Item index -> (pair level, batch, head, split).  Longest-processing-time order:
+// pair index descending (under a causal mask later pairs see more key blocks), then
+// (batch, head, split).  Taken level by level, the items running at one time span
+// every (batch, head), whose K/V streams together outgrow L2.  So a static schedule
+// may first run bands (set by the host): `band_levels` consecutive levels of one
+// (batch, head, split), then the next (batch, head, split).  The host sizes a causal
+// band so that the snake's paired rounds still balance (see fa_api.cu) and leaves the
+// last levels, the small items, in plain LPT order.  Query heads sharing a K/V head
+// (grouped-query attention) are consecutive items, so they stream the same K/V at
+// about the same time and share it in L2.
 template <bool PAIR>
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int w, uint32_t rank) {
     Item it;
@@ -225,8 +235,20 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int w, uint32_t 
     // r = i * G + g.  it.h is then the group's first query head.
     const int G = p.pack;
     const int per_m = p.batch * p.item_heads * p.n_splits;
-    const int mp = p.n_mpairs - 1 - w / per_m;
-    const int r = w % per_m;
+    int level, r;  // level 0 = the last pair (the most key blocks under a causal mask)
+    if (w < p.band_items) {  // band_levels consecutive levels of one (batch, head, split)
+        const int per_band = p.band_levels * per_m;
+        const int bi = w / per_band;
+        const int rem = w - bi * per_band;
+        r = rem / p.band_levels;
+        level = bi * p.band_levels + (rem - r * p.band_levels);
+    } else {  // level by level, all (batch, head, split) of a level together
+        const int w2 = w - p.band_items;
+        const int l2 = w2 / per_m;
+        level = p.band_lv + l2;
+        r = w2 - l2 * per_m;
+    }
+    const int mp = p.n_mpairs - 1 - level;
     it.split = r % p.n_splits;
     const int bh = r / p.n_splits;
     it.h = (bh % p.item_heads) * G;

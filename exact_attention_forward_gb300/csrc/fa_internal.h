@@ -44,6 +44,10 @@ struct FwdParams {
     int n_splits;               // key-range splits (1 = none)
     int blocks_per_split;       // key blocks per split
     int n_items;                // n_mpairs * batch * item_heads * n_splits
+    int band_levels;            // static order: the first band_items items run in bands of
+    int band_items;             //   band_levels consecutive pair levels per (batch, head), so
+    int band_lv;                //   CTAs running at the same time share K/V in L2; band_lv =
+                                //   banded levels (band_items / items per level); 0: none
     float scale_log2;           // softmax_scale * log2(e)
     int causal, varlen, split;
     int greedy;                 // items handed out by the device counter (varlen) or a static snake

@@ -170,8 +170,9 @@ FA_API fa_status fa_fwd_fp8(const void* q, const void* k, const void* v,
  *   head_dim = head_dim_v = 128, no workspace: no key splits).
  * Same outputs, layouts and validation as fa_fwd_gqa.  FA_ERR_UNSUPPORTED for
  * head_dim != 128, or when no cluster of two CTAs fits on the device.  The
- * work items (512 query rows of one batch and head) follow a static
- * longest-first order, also for varlen.
+ * work items (512 query rows of one batch and head) follow a static order,
+ * also for varlen: longest first, for fixed lengths grouped by (batch, head)
+ * where that keeps the CTAs' loads balanced.
  */
 FA_API fa_status fa_fwd_2cta(const void* q, const void* k, const void* v,
                              void* o, float* lse,

@@ -1,8 +1,9 @@
 """GPU: behaviour that depends on how work is handed out and on state kept between
 launches -- the greedy varlen scheduler's per-launch device counters (more launches
 than counter slots, two streams at once, recovery after an aborted launch), CUDA graph
-capture and replay, and extreme shapes (a thousand tiny sequences, a 256K key range,
-thousands of one-tile problems), each checked against the fp64 oracle.
+capture and replay, extreme shapes (a thousand tiny sequences, a 256K key range,
+thousands of one-tile problems), and the L2-banded static item orders, each checked
+against the fp64 oracle.
 """
 import numpy as np
 import pytest
@@ -163,3 +164,29 @@ def test_thousands_of_one_tile_problems():
                                            softmax_scale=128 ** -0.5, causal=True)
     og, lg = gather_rows(o, lse, rows)
     compare(og, lg, o_ref, lse_ref, what="64 x 32 one-tile problems")
+
+
+# Fixed-length static schedules run in L2 bands (consecutive query-tile pairs of one
+# (batch, head) side by side).  On a 152-SM GB300 these shapes take the band layouts
+# that the large workloads use, at sizes the oracle checks in full: a causal band of
+# 2 levels (152 items per level), a causal band of 4 levels with a partial last round
+# and the K/V heads shared by groups of 4 query heads, and head-major orders without a
+# causal mask (one CTA per SM, and on CTA pairs).  Whatever the order, every item must
+# be computed exactly once.
+@pytest.mark.parametrize("shape", [
+    dict(batch=2, heads=76, heads_k=76, s=1024, d=64, causal=True, pair=False),
+    dict(batch=1, heads=76, heads_k=19, s=1792, d=128, causal=True, pair=False),
+    dict(batch=3, heads=20, heads_k=20, s=1536, d=64, causal=False, pair=False),
+    dict(batch=3, heads=20, heads_k=5, s=1536, d=128, causal=False, pair=True),
+], ids=["causal-2-levels", "causal-4-levels-gqa", "noncausal-head-major",
+        "noncausal-head-major-pair"])
+def test_l2_band_orders(shape):
+    s, d = shape["s"], shape["d"]
+    x = inputs.make_random(shape["batch"], shape["heads"], s, s, d, seed=521,
+                           heads_k=shape["heads_k"])
+    scale = d ** -0.5
+    o, lse = run_gpu(x, causal=shape["causal"], softmax_scale=scale, workspace=None,
+                     cta_pair=shape["pair"])
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=scale,
+                                      causal=shape["causal"])
+    compare(o, lse, o_ref, lse_ref, what=f"banded order {shape}")
