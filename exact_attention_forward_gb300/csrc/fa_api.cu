@@ -561,6 +561,8 @@ fa_status fwd_impl(const FwdArgs& a) {
     return FA_OK;
 }
 
+fa_status set_error_detail(fa_status status, const char* msg) { return fail(status, "%s", msg); }
+
 }  // namespace fa
 
 using namespace fa;

@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fa.h"
+
 namespace fa {
 
 // Everything a forward launch needs besides the three TMA tensor maps.
@@ -85,5 +87,8 @@ cudaError_t launch_combine(const float* ws_o, const float* ws_lse, void* o, floa
                            int batch, int heads, int seqlen_q, int dv, int n_splits,
                            cudaStream_t s);
 uint32_t* device_error_word();  // address of the device error word (current device)
+// Records `msg` as this thread's fa_last_error_detail() and returns `status` (for entry
+// points outside fa_api.cu).
+fa_status set_error_detail(fa_status status, const char* msg);
 
 }  // namespace fa

@@ -26,6 +26,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_internal.h"
 
 namespace {
 
@@ -47,14 +48,17 @@ extern "C" fa_status fa_fwd_static_workspace(
     fa_dtype dtype, const float* q_descale, const float* k_descale, const float* v_descale,
     void* stream) {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return fa::set_error_detail(FA_ERR_CUDA, "no usable current CUDA device");
     void* scratch = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!g_scratch_addr[dev]) {
             void* addr = nullptr;
             cudaError_t e = cudaGetSymbolAddress(&addr, g_fa_static_scratch);
-            if (e != cudaSuccess || addr == nullptr) return FA_ERR_CUDA;
+            if (e != cudaSuccess || addr == nullptr)
+                return fa::set_error_detail(FA_ERR_CUDA,
+                                            "device address of the static scratch unavailable");
             g_scratch_addr[dev] = addr;
         }
         scratch = g_scratch_addr[dev];

@@ -178,3 +178,18 @@ def test_cta_pair_validation(lib, kw, code):
 
 def test_cta_pair_empty_problem_is_ok_without_a_device(lib):
     assert pair(lib, batch=0) == fa.FA_OK
+
+
+def test_static_workspace_without_a_device_says_why(lib):
+    # with no usable device the entry point that allocates nothing fails before any device
+    # work, with FA_ERR_CUDA and a detail message (never a stale or empty one)
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present: this checks the no-device path")
+    lib.fa_fwd(None, P, P, P, P, 1, 1, 128, 128, None, None, 0, 0, 128, 128, 0.1, 0, 0,
+               None, None, None, None, 0, None)  # leaves an unrelated detail behind
+    st = lib.fa_fwd_static_workspace(P, P, P, P, P, 1, 1, 128, 128, 128, 128, 0.1, 0, 0,
+                                     None, None, None, None)
+    assert st == fa.FA_ERR_CUDA
+    detail = lib.fa_last_error_detail()
+    assert b"no usable current CUDA device" in detail or b"static scratch" in detail, detail
