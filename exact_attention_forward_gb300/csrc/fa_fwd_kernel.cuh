@@ -58,6 +58,8 @@
 //     tile pairs of one (batch, head) side by side (all of them without a causal
 //     mask; a band sized to keep the snake balanced, then plain LPT, under one),
 //     so the CTAs running at one time read few heads' K/V and find it in L2;
+//     without a causal mask, a last round holding at most half as many pairs as
+//     CTAs runs its pairs as single tiles, two items each;
 //   * key/value-cache launches with few, long items (decoding) use a balanced
 //     plan instead: every producer reads the cache lengths, and each CTA takes
 //     an equal share of the key blocks of all items, concatenated, as pieces
@@ -230,6 +232,12 @@ template <bool PAIR>
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int w, uint32_t rank) {
     Item it;
     it.fill = 0;
+    int half = -1;  // a single query tile (0 or 1) of a tile pair item, or -1: the pair
+    if (!PAIR && p.half_from > 0 && w >= p.half_from) {
+        const int d = w - p.half_from;
+        half = d & 1;
+        w = p.half_from + (d >> 1);
+    }
     // packed grouped-query mode (p.pack = G > 1): an item serves one K/V head, and its
     // tile rows are (query row, query head of the group) pairs, row-major: packed row
     // r = i * G + g.  it.h is then the group's first query head.
@@ -273,6 +281,16 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int w, uint32_t 
     const int nblk = (it.sk + kBN - 1) / kBN;
     it.n_lo = it.split * p.blocks_per_split;
     set_tile_ranges<PAIR>(p, it, mp, min(nblk, it.n_lo + p.blocks_per_split), rank);
+    if (half >= 0) {  // run tile `half` alone, as tile 0; tile 1 does nothing
+        if (half == 1) {
+            it.m0[0] = it.m0[1];
+            it.active[0] = it.active[1];
+            it.n_hi_t[0] = it.n_hi_t[1];
+        }
+        it.active[1] = false;
+        it.n_hi_t[1] = it.n_lo;
+        it.n_hi = max(it.n_hi_t[0], it.n_lo);
+    }
     return it;
 }
 

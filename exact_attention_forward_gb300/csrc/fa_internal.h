@@ -50,6 +50,11 @@ struct FwdParams {
     int band_items;             //   band_levels consecutive pair levels per (batch, head), so
     int band_lv;                //   CTAs running at the same time share K/V in L2; band_lv =
                                 //   banded levels (band_items / items per level); 0: none
+    int half_from;              // static order, one CTA per tile pair: items from this index
+                                //   on are single query tiles, two per tile pair (index
+                                //   half_from + 2i + t: tile t of pair item half_from + i), so
+                                //   a part-filled last round spreads over more CTAs; n_items
+                                //   counts them; 0: none
     float scale_log2;           // softmax_scale * log2(e)
     int causal, varlen, split;
     int greedy;                 // items handed out by the device counter (varlen) or a static snake

@@ -190,3 +190,25 @@ def test_l2_band_orders(shape):
     o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=scale,
                                       causal=shape["causal"])
     compare(o, lse, o_ref, lse_ref, what=f"banded order {shape}")
+
+
+# Without a causal mask, a static schedule whose last round holds at most half as many
+# tile pairs as there are CTAs runs that round's pairs as single tiles (two items each).
+# On a 152-SM GB300 these shapes take that path: 160 pairs (a tail of 8), 212 pairs (a
+# tail of 60) whose last level's second tile holds 4 rows or lies wholly past the end,
+# grouped K/V heads, head dim 64 and FP8.
+@pytest.mark.parametrize("shape", [
+    dict(heads=40, heads_k=40, s=1000, d=128, dtype="bf16"),
+    dict(heads=53, heads_k=53, s=900, d=64, dtype="bf16"),
+    dict(heads=52, heads_k=13, s=800, d=128, dtype="bf16"),
+    dict(heads=40, heads_k=40, s=1000, d=128, dtype="e4m3"),
+], ids=["tail-8", "tail-60-ragged", "tail-gqa-empty-tile", "tail-fp8"])
+def test_single_tile_tail(shape):
+    s, d = shape["s"], shape["d"]
+    x = inputs.make_random(1, shape["heads"], s, s, d, seed=541, heads_k=shape["heads_k"],
+                           dtype=shape["dtype"])
+    scale = d ** -0.5
+    o, lse = run_gpu(x, causal=False, softmax_scale=scale, workspace=None)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=scale,
+                                      descale=x["descale"])
+    compare(o, lse, o_ref, lse_ref, dtype=shape["dtype"], what=f"single-tile tail {shape}")
