@@ -59,6 +59,25 @@ def _flops(w, x) -> float:
     return tot / 2 if w.causal else tot
 
 
+# Issue limit of exp2 on the MUFU (SFU) of a GB300 SM: 32 per clock, from the ncu XU-pipe
+# utilisation of the causal 8K launch (30 % active) against its exp2 count.
+MUFU_EXP2_PER_CLK_PER_SM = 32
+
+
+def exp2_bound(flops: float, head_dim: int, tensor_peak_tflops: float, sms: int,
+               sm_mhz: float) -> dict:
+    """The two ceilings of a pass through the forward kernel: the tensor pipe (the
+    algorithmic FLOPs at the tensor peak) and the MUFU (one exp2 per visible (query row,
+    key) pair, i.e. FLOPs / (4 D), at its issue limit).  The larger time is attainable."""
+    exps = flops / (4.0 * head_dim)
+    exp2_ms = exps / (MUFU_EXP2_PER_CLK_PER_SM * sms * sm_mhz * 1e6) * 1e3
+    tensor_ms = flops / (tensor_peak_tflops * 1e12) * 1e3
+    return {"exp2_per_launch": exps, "exp2_per_clk_per_sm": MUFU_EXP2_PER_CLK_PER_SM,
+            "sms": sms, "sm_mhz": sm_mhz, "exp2_ms": exp2_ms, "tensor_ms": tensor_ms,
+            "attainable_ms": max(exp2_ms, tensor_ms),
+            "limit": "tensor" if tensor_ms >= exp2_ms else "exp2"}
+
+
 def _bytes(w, x) -> float:
     """Compulsory HBM bytes of one pass: Q, K, V read once; O (bf16) and LSE (fp32) written.
     Cache workloads: the filled cache rows each sequence uses are read once, the new rows
@@ -517,6 +536,10 @@ def run_gpu(args, w):
                 "peak_source": src,
                 "frac_of_sustained": (achieved / peaks.get("bf16_tflops_sustained", peak)
                                       if bound == "tensor" and not fp8 else None)}
+    if bound == "tensor":
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        sm_mhz = clocks.get("sm_mhz") or peaks.get("sm_max_mhz") or 2070.0
+        roofline["exp2_bound"] = exp2_bound(flops, w.head_dim, peak, sms, sm_mhz)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
