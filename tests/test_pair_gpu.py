@@ -3,7 +3,7 @@ slots, each CTA of a cluster loading half of every K/V block) against the fp64
 oracle, on the shapes that exercise what differs from the one-CTA kernel: work
 items of 512 query rows whose second CTA's rows run past the sequence end, key
 blocks that one CTA of a slot sees fully masked under a causal mask, grouped
-K/V heads, varlen batches with empty sequences, and the full-size workloads.
+K/V heads, varlen batches with empty sequences, and the full-size workloads (every row).
 """
 import numpy as np
 import pytest
@@ -12,7 +12,7 @@ import torch
 import oracle
 import exact_attention_forward_gb300 as fa
 from exact_attention_forward_gb300 import inputs
-from parity_util import compare, gather_rows, run_gpu, sample_rows
+from parity_util import compare, oracle_abs_v, oracle_full, run_gpu, workload_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -71,40 +71,22 @@ def test_pair_varlen_small_full(causal):
     compare(o, lse, o_ref, lse_ref, what=f"pair varlen causal={causal}")
 
 
-@pytest.fixture(scope="module")
-def inputs_8k():
-    return inputs.make_inputs(inputs.WORKLOADS["bf16_causal_8k"])
-
-
 @pytest.mark.parametrize("name", ["bf16_causal_8k", "bf16_noncausal_8k"])
-def test_pair_8k_workloads_sampled(name, inputs_8k):
+def test_pair_8k_workloads_full(name):
     w = inputs.WORKLOADS[name]
-    x = inputs_8k
+    x = workload_inputs("bf16_causal_8k")  # both workloads attend over the same inputs
     o, lse = run_gpu(x, causal=w.causal, softmax_scale=w.softmax_scale, cta_pair=True)
-    rows = sample_rows(w.batch, w.heads, w.seqlen_q, 256, seed=55)
-    o_ref, lse_ref = oracle.attention_rows(x["q"], x["k"], x["v"], rows,
-                                           softmax_scale=w.softmax_scale, causal=w.causal)
-    og, lg = gather_rows(o, lse, rows)
-    compare(og, lg, o_ref, lse_ref, what=f"pair {name}")
-    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
-    # the one-CTA kernel computes the same attention
-    o1, lse1 = run_gpu(x, causal=w.causal, softmax_scale=w.softmax_scale)
-    assert np.abs(o1 - o).max() <= 2e-2 and np.abs(lse1 - lse).max() <= 1e-3
+    o_ref, lse_ref = oracle_full(name)
+    compare(o, lse, o_ref, lse_ref, what=f"pair {name}",
+            o_abs_v=oracle_abs_v(x, softmax_scale=w.softmax_scale, causal=w.causal))
 
 
-def test_pair_varlen_workload_sampled():
+def test_pair_varlen_workload_full():
     w = inputs.WORKLOADS["bf16_varlen_causal"]
-    x = inputs.make_inputs(w)
-    sq, sk = x["seqlens"]
-    cu_q = x["cu_seqlens_q"].numpy()
+    x = workload_inputs(w.name)
     o, lse = run_gpu(x, causal=w.causal, softmax_scale=w.softmax_scale, cta_pair=True)
-    rows = sample_rows(len(sq), w.heads, None, 512, seed=56, seqlens_q=sq)
-    o_ref, lse_ref = oracle.attention_rows(x["q"], x["k"], x["v"], rows,
-                                           softmax_scale=w.softmax_scale, causal=w.causal,
-                                           cu_seqlens_q=x["cu_seqlens_q"],
-                                           cu_seqlens_k=x["cu_seqlens_k"])
-    og, lg = gather_rows(o, lse, rows, varlen=True, cu_q=cu_q)
-    compare(og, lg, o_ref, lse_ref, what=f"pair {w.name}")
+    o_ref, lse_ref = oracle_full(w.name)
+    compare(o, lse, o_ref, lse_ref, what=f"pair {w.name}")
 
 
 def test_pair_rejects_unbuilt_configurations():

@@ -12,7 +12,7 @@ import torch
 import oracle
 import exact_attention_forward_gb300 as fa
 from exact_attention_forward_gb300 import inputs
-from parity_util import compare, gather_rows, run_gpu, sample_rows, to_dev
+from parity_util import compare, lse_shape_of, nan_outputs, run_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -46,7 +46,8 @@ def test_varlen_launches_wrap_the_counter_slots():
     # 300 launches > 256 counter slots: every slot is reused after its last CTA returned it
     # to zero; a slot left non-zero would skip items and change the result
     x, d, kw = _varlen_case([700, 33, 1200, 5, 400], seed=501)
-    o0, l0 = fa.fwd(d["q"], d["k"], d["v"], **kw)
+    o0, l0 = nan_outputs(d["q"], d["v"], lse_shape_of(x))
+    fa.fwd(d["q"], d["k"], d["v"], out=o0, lse=l0, **kw)
     torch.cuda.synchronize()
     compare(*_np(o0, l0), *_varlen_ref(x), what="first varlen launch")
     o0, l0 = o0.clone(), l0.clone()
@@ -63,11 +64,14 @@ def test_varlen_on_two_streams_at_once():
     xb, db, kwb = _varlen_case([64, 2000, 3, 700, 700], heads=6, seed=503)
     sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
     torch.cuda.synchronize()
+    oa, la = nan_outputs(da["q"], da["v"], lse_shape_of(xa))
+    ob, lb = nan_outputs(db["q"], db["v"], lse_shape_of(xb))
+    torch.cuda.synchronize()
     for _ in range(20):
         with torch.cuda.stream(sa):
-            oa, la = fa.fwd(da["q"], da["k"], da["v"], stream=sa, **kwa)
+            fa.fwd(da["q"], da["k"], da["v"], stream=sa, out=oa, lse=la, **kwa)
         with torch.cuda.stream(sb):
-            ob, lb = fa.fwd(db["q"], db["k"], db["v"], stream=sb, **kwb)
+            fa.fwd(db["q"], db["k"], db["v"], stream=sb, out=ob, lse=lb, **kwb)
     torch.cuda.synchronize()
     assert fa.device_error(clear=True)[0] == fa.FA_OK
     compare(*_np(oa, la), *_varlen_ref(xa), what="stream a")
@@ -88,7 +92,8 @@ def test_counter_slot_recovers_after_an_aborted_launch():
     ref = _varlen_ref(x)
     first = None
     for i in range(260):
-        o, lse = fa.fwd(d["q"], d["k"], d["v"], **kw)
+        o, lse = nan_outputs(d["q"], d["v"], lse_shape_of(x))
+        fa.fwd(d["q"], d["k"], d["v"], out=o, lse=lse, **kw)
         if first is None:
             torch.cuda.synchronize()
             compare(*_np(o, lse), *ref, what="after the aborted launch")
@@ -113,7 +118,7 @@ def test_cuda_graph_capture_and_replay(varlen):
     # the summation order); also warms the library's per-device state before capture
     o_e, l_e = fa.fwd(q, k, v, workspace=None, **kw)
     torch.cuda.synchronize()
-    out, lse = torch.empty_like(o_e), torch.empty_like(l_e)
+    out, lse = nan_outputs(q, v, tuple(l_e.shape))
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -122,7 +127,8 @@ def test_cuda_graph_capture_and_replay(varlen):
             fa.fwd(q, k, v, out=out, lse=lse, workspace=None, stream=s, **kw)
     torch.cuda.current_stream().wait_stream(s)
     for _ in range(3):
-        out.zero_()
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, o_e) and torch.equal(lse, l_e)
@@ -149,21 +155,16 @@ def test_256k_key_range():
     x = inputs.make_random(1, 1, 64, 262144, 128, seed=509)
     assert fa.num_splits(1, 1, 64, 262144) > 100
     o, lse = run_gpu(x, causal=False, softmax_scale=128 ** -0.5)
-    rows = sample_rows(1, 1, 64, 8, seed=510)
-    o_ref, lse_ref = oracle.attention_rows(x["q"], x["k"], x["v"], rows,
-                                           softmax_scale=128 ** -0.5)
-    og, lg = gather_rows(o, lse, rows)
-    compare(og, lg, o_ref, lse_ref, what="256K keys")
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=128 ** -0.5)
+    compare(o, lse, o_ref, lse_ref, what="256K keys")
 
 
 def test_thousands_of_one_tile_problems():
     x = inputs.make_random(64, 32, 128, 128, 128, seed=511)
     o, lse = run_gpu(x, causal=True, softmax_scale=128 ** -0.5)
-    rows = sample_rows(64, 32, 128, 512, seed=512)
-    o_ref, lse_ref = oracle.attention_rows(x["q"], x["k"], x["v"], rows,
-                                           softmax_scale=128 ** -0.5, causal=True)
-    og, lg = gather_rows(o, lse, rows)
-    compare(og, lg, o_ref, lse_ref, what="64 x 32 one-tile problems")
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=128 ** -0.5,
+                                      causal=True)
+    compare(o, lse, o_ref, lse_ref, what="64 x 32 one-tile problems")
 
 
 # Fixed-length static schedules run in L2 bands (consecutive query-tile pairs of one
