@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--cta-pair]
     python bench.py --impl reference ...     # the fp64 CPU oracle, timed on host cores
+    python bench.py --microbench             # ex2 and tcgen05 throughput per SM clock
 
 Prints ONE JSON line (rank 0).  A step is one forward pass over the whole
 workload (default: bf16, causal, B=2 H=32 S=8192 D=128, inputs 2*N(0,1)):
@@ -59,23 +60,101 @@ def _flops(w, x) -> float:
     return tot / 2 if w.causal else tot
 
 
-# Issue limit of exp2 on the MUFU (SFU) of a GB300 SM: 32 per clock, from the ncu XU-pipe
-# utilisation of the causal 8K launch (30 % active) against its exp2 count.
-MUFU_EXP2_PER_CLK_PER_SM = 32
-
-
 def exp2_bound(flops: float, head_dim: int, tensor_peak_tflops: float, sms: int,
-               sm_mhz: float) -> dict:
+               sm_mhz: float, exp2_per_clk_per_sm: float) -> dict:
     """The two ceilings of a pass through the forward kernel: the tensor pipe (the
     algorithmic FLOPs at the tensor peak) and the MUFU (one exp2 per visible (query row,
-    key) pair, i.e. FLOPs / (4 D), at its issue limit).  The larger time is attainable."""
+    key) pair, i.e. FLOPs / (4 D), at the ex2 rate measured by the throughput probe).
+    The larger time is attainable."""
     exps = flops / (4.0 * head_dim)
-    exp2_ms = exps / (MUFU_EXP2_PER_CLK_PER_SM * sms * sm_mhz * 1e6) * 1e3
+    exp2_ms = exps / (exp2_per_clk_per_sm * sms * sm_mhz * 1e6) * 1e3
     tensor_ms = flops / (tensor_peak_tflops * 1e12) * 1e3
-    return {"exp2_per_launch": exps, "exp2_per_clk_per_sm": MUFU_EXP2_PER_CLK_PER_SM,
+    return {"exp2_per_launch": exps, "exp2_per_clk_per_sm": exp2_per_clk_per_sm,
             "sms": sms, "sm_mhz": sm_mhz, "exp2_ms": exp2_ms, "tensor_ms": tensor_ms,
             "attainable_ms": max(exp2_ms, tensor_ms),
             "limit": "tensor" if tensor_ms >= exp2_ms else "exp2"}
+
+
+# ------------------------------------------------------------------ throughput probes
+def _microbench_lib():
+    import ctypes
+    from exact_attention_forward_gb300 import _build
+    lib = ctypes.CDLL(_build.build_microbench())
+    vp, i32, i64, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_ulonglong
+    lib.fa_mb_ex2.restype = i32
+    lib.fa_mb_ex2.argtypes = [i32, i32, vp, vp, vp]
+    lib.fa_mb_ex2_per_cta.restype = i64
+    lib.fa_mb_ex2_per_cta.argtypes = [i32]
+    lib.fa_mb_mma.restype = i32
+    lib.fa_mb_mma.argtypes = [i32, i32, i32, i32, vp, vp, u64, vp]
+    lib.fa_mb_mma_flops_per_cta.restype = i64
+    lib.fa_mb_mma_flops_per_cta.argtypes = [i32, i32, i32]
+    return lib
+
+
+def _per_sm_rates(units_per_cta: float, cycles) -> dict:
+    rates = sorted(units_per_cta / float(c) for c in cycles if c > 0)
+    return {"median": statistics.median(rates), "min": rates[0], "max": rates[-1]}
+
+
+def measure_ex2_rate(dev, iters: int = 2048) -> dict:
+    """ex2.approx.ftz.f32 per SM clock (one 1024-thread CTA per SM, clock64-timed)."""
+    import torch
+    lib = _microbench_lib()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    cyc = torch.zeros(sms, dtype=torch.int64, device=dev)
+    sink = torch.zeros(1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    for _ in range(2):  # the first launch also loads the module
+        rc = lib.fa_mb_ex2(sms, iters, cyc.data_ptr(), sink.data_ptr(), stream)
+        if rc != 0:
+            raise RuntimeError(f"fa_mb_ex2 launch failed ({rc})")
+    torch.cuda.synchronize(dev)
+    return _per_sm_rates(lib.fa_mb_ex2_per_cta(iters), cyc.cpu().tolist())
+
+
+def measure_mma_rate(dev, n: int, fp8: bool, iters: int = 2048) -> dict:
+    """tcgen05.mma FLOP per SM clock, M = 128, N = n, one issuing thread per SM."""
+    import torch
+    lib = _microbench_lib()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    cyc = torch.zeros(sms, dtype=torch.int64, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    for _ in range(2):
+        rc = lib.fa_mb_mma(sms, n, int(fp8), iters, cyc.data_ptr(), err.data_ptr(),
+                           2_000_000_000, stream)
+        if rc != 0:
+            raise RuntimeError(f"fa_mb_mma launch failed ({rc})")
+    torch.cuda.synchronize(dev)
+    if int(err.item()) != 0:
+        raise RuntimeError("fa_mb_mma: a bounded wait ran out")
+    return _per_sm_rates(lib.fa_mb_mma_flops_per_cta(n, int(fp8), iters), cyc.cpu().tolist())
+
+
+def run_microbench(args):
+    """One JSON line: ex2 and tcgen05 rates per SM clock, and what they give at the SM
+    clock sampled while they ran."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    ex2 = measure_ex2_rate(dev)
+    mma = {}
+    for n, fp8 in ((64, False), (128, False), (256, False), (128, True), (256, True)):
+        mma[f"{'e4m3' if fp8 else 'bf16'}_m128_n{n}"] = measure_mma_rate(dev, n, fp8)
+    clocks = sampler.stop()
+    mhz = clocks.get("sm_mhz") or 2070.0
+    line = {"microbench": "ex2 / tcgen05 throughput", "sms": sms, "clocks": clocks,
+            "ex2_per_clk_per_sm": ex2,
+            "ex2_per_s_chip_at_sm_mhz": ex2["median"] * sms * mhz * 1e6,
+            "mma_flop_per_clk_per_sm": mma,
+            "mma_tflops_chip_at_sm_mhz": {k: v["median"] * sms * mhz * 1e6 / 1e12
+                                          for k, v in mma.items()}}
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 def _bytes(w, x) -> float:
@@ -102,6 +181,8 @@ def _source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_forward_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
+        if not os.path.isfile(os.path.join(csrc, f)):  # (the throughput probes' folder)
+            continue
         with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             text = fh.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
@@ -298,12 +379,18 @@ def run_reference(args, w):
         secs += dt
         rows_total += n
     value = flops / secs / 1e12
+    full = _flops(w, x)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+        # one step = the whole workload; the oracle computes a sample of its rows per step,
+        # so the time of a whole step follows from the sampled rate
+        "ms_per_step": full / (value * 1e12) * 1e3,
+        "sample_ms_per_step": 1e3 * secs / max(1, args.steps),
+        "sample_fraction_per_step": flops / max(1, args.steps) / full,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": _config(w, "n/a (CPU)"),
+        "config": _config(w),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _oracle_threads(),
                          "kind": "oracle",
                          "sample": f"{rows_total} seeded random query rows of {w.name} "
@@ -315,11 +402,16 @@ def run_reference(args, w):
     return 0
 
 
-def _config(w, l2):
+L2_NOTE = ("GPU arm: L2 flushed between timed steps (256 MiB write + 256 MiB read, untimed); "
+           "CPU oracle arm: not applicable")
+
+
+def _config(w):
+    """The workload, identical in both arms' lines."""
     c = {"workload": w.name, "batch": w.batch, "heads": w.heads, "heads_k": w.kv_heads,
          "seqlen_q": w.seqlen_q,
          "seqlen_k": w.seqlen_k, "head_dim": w.head_dim, "causal": w.causal,
-         "input_dtype": w.dtype, "values": f"{w.amp:g}*N(0,1) seed {w.seed}", "l2": l2}
+         "input_dtype": w.dtype, "values": f"{w.amp:g}*N(0,1) seed {w.seed}", "l2": L2_NOTE}
     if w.varlen:
         c["varlen"] = f"{w.n_seqs} seqs U{{1..{w.seqlen_q}}} + {len(w.empty_k_at)} with Sk=0"
     if w.cache_new:
@@ -539,15 +631,23 @@ def run_gpu(args, w):
     if bound == "tensor":
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         sm_mhz = clocks.get("sm_mhz") or peaks.get("sm_max_mhz") or 2070.0
-        roofline["exp2_bound"] = exp2_bound(flops, w.head_dim, peak, sms, sm_mhz)
+        try:  # the ex2 rate, measured now by the throughput probe (a few ms)
+            ex2 = measure_ex2_rate(dev)
+            roofline["exp2_bound"] = exp2_bound(flops, w.head_dim, peak, sms, sm_mhz,
+                                                ex2["median"])
+            roofline["exp2_bound"]["exp2_rate_source"] = (
+                "measured in this run: ex2.approx.ftz.f32 throughput probe, one 1024-thread "
+                "CTA per SM, clock64-timed (median over SMs)")
+        except Exception as exc:  # keep the line; say why the second ceiling is missing
+            roofline["exp2_bound"] = {"unavailable": f"ex2 probe failed: {exc}"}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if not fp8 else "e4m3", "data": "synthetic",
-        "config": dict(_config(w, "flushed between timed steps (256 MiB write + 256 MiB read, untimed)"),
-                       kernel="cta_pair (clusters of 2, cta_group::2)" if pair else "one CTA per SM"),
+        "config": _config(w),
+        "kernel": "cta_pair (clusters of 2, cta_group::2)" if pair else "one CTA per SM",
         "clocks": clocks, "e2e": e2e,
         # per step: the forward kernel, the split merge when the key range is split, and the
         # cache-append copy kernel when a call appends more than 4 rows per sequence (fewer
@@ -585,7 +685,11 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cta-pair", action="store_true",
                     help="time the CTA-pair kernel (fa_fwd_2cta) instead of the one-CTA kernel")
+    ap.add_argument("--microbench", action="store_true",
+                    help="measure the ex2 and tcgen05 throughput per SM clock and exit")
     args = ap.parse_args(argv)
+    if args.microbench:
+        return run_microbench(args)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     from exact_attention_forward_gb300 import inputs

@@ -18,6 +18,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "_fa_gb300.so")
+# throughput probes of the ex2 unit and the tensor pipe (measurement only; not the product path)
+MB_SRC = os.path.join(CSRC, "microbench", "fa_microbench.cu")
+MB_LIB = os.path.join(HERE, "_fa_microbench.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["fa_api.cu", "fa_fwd_bf16_d64.cu", "fa_fwd_bf16_d128.cu", "fa_fwd_e4m3_d128.cu",
            "fa_fwd_pair_bf16_d128.cu", "fa_static_ws.cu", "fa_append_kv.cu"]
@@ -29,8 +32,29 @@ def _nvcc():
 
 
 def _deps():
-    return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [
-        os.path.join(ROOT, "include", "fa.h")]
+    return [os.path.join(CSRC, f) for f in os.listdir(CSRC)
+            if os.path.isfile(os.path.join(CSRC, f))] + [os.path.join(ROOT, "include", "fa.h")]
+
+
+def build_microbench(force: bool = False) -> str:
+    """Build _fa_microbench.so (one translation unit) next to the main library."""
+    deps = [MB_SRC, os.path.join(CSRC, "sm103_ptx.cuh"),
+            os.path.join(ROOT, "include", "fa_microbench.h")]
+    if (not force and os.path.exists(MB_LIB)
+            and os.path.getmtime(MB_LIB) >= max(os.path.getmtime(d) for d in deps)):
+        return MB_LIB
+    os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock_mb"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        tmp = MB_LIB + f".tmp{os.getpid()}"
+        cmd = [_nvcc()] + ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+                                  "-Xcompiler", "-fvisibility=hidden", "-I",
+                                  os.path.join(ROOT, "include"), "-shared", MB_SRC, "-o", tmp]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {MB_SRC}:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, MB_LIB)
+    return MB_LIB
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: str = LIB,

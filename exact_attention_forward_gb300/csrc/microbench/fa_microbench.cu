@@ -1,0 +1,170 @@
+// fa_microbench.cu -- throughput probes of the two units that bound the attention
+// forward kernel on this GPU, built as a library of its own (_fa_microbench.so):
+//
+//  * the MUFU exponential: ex2.approx.ftz.f32 issued by every thread of one
+//    1024-thread CTA per SM, eight independent dependency chains per thread, so the
+//    unit's issue rate (not its latency) sets the time.  Result: ex2 per SM clock.
+//  * the tensor pipe: one thread per SM issuing tcgen05.mma (cta_group::1, A and B
+//    from 128-byte-swizzled shared memory, fp32 accumulator in Tensor Memory) back to
+//    back, M = 128 and N = 64 / 128 / 256 with bf16 (kind::f16, K = 16 per MMA) or
+//    e4m3 (kind::f8f6f4, K = 32), one commit at the end.  Result: FLOP per SM clock.
+//
+// Each CTA times itself with clock64 (SM cycles), so the rates do not depend on the
+// clock the GPU happens to run at.  Why they matter: the page "Dissecting the SM_120
+// Microarchitecture" (section 11.2, Fig. 12) finds the softmax's exponentials, not the
+// MMAs, to dominate a key block of fused attention on a GPU without Tensor Memory; the
+// attainable time of a forward pass is the larger of (exponentials / ex2 rate) and
+// (FLOPs / tensor rate), and both rates are measured here rather than assumed.
+//
+// Every wait is bounded by %globaltimer; a wait that runs out sets *err and the CTA
+// still waits (bounded again) for its MMAs before freeing Tensor Memory.
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "fa_microbench.h"
+#include "../sm103_ptx.cuh"
+
+namespace {
+
+using namespace fa;
+
+constexpr int kEx2Threads = 1024;
+constexpr int kEx2Chains = 8;
+
+__global__ void __launch_bounds__(kEx2Threads, 1)
+    mb_ex2_kernel(int iters, unsigned long long* cycles, float* sink) {
+    float x[kEx2Chains];
+#pragma unroll
+    for (int u = 0; u < kEx2Chains; ++u) x[u] = 0.25f + 0.01f * (float)((threadIdx.x + u) & 31);
+    __syncthreads();
+    const unsigned long long t0 = clock64();
+#pragma unroll 1
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int u = 0; u < kEx2Chains; ++u) x[u] = ex2_approx(-x[u]);  // stays in (0.5, 1)
+    }
+    __syncthreads();
+    const unsigned long long t1 = clock64();
+    if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
+    float s = 0.f;
+#pragma unroll
+    for (int u = 0; u < kEx2Chains; ++u) s += x[u];
+    if (s == -1.0f) sink[threadIdx.x] = s;  // never true; keeps the chains alive
+}
+
+constexpr int kMmaSmem = 120 * 1024;  // > half the SM's shared memory: one CTA per SM
+
+template <int N, bool FP8>
+__global__ void __launch_bounds__(128, 1)
+    mb_mma_kernel(int iters, unsigned long long* cycles, uint32_t* err, unsigned long long limit_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    // A: 128 rows x 128 bytes, B: N rows x 128 bytes (one swizzle atom column each, i.e.
+    // K = 64 bf16 or 128 e4m3 elements: four MMAs of K = 16 / 32), zeros
+    uint8_t* a = smem;
+    uint8_t* b = smem + 128 * 128;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(b + N * 128);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+    for (int i = threadIdx.x; i < (128 + N) * 128 / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(bar), 1);
+        fence_barrier_init();
+    }
+    fence_proxy_async_smem();  // the zeros are visible to the tensor pipe
+    if (threadIdx.x < 32) {
+        tmem_alloc(smem_u32(tslot), 512);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    if (threadIdx.x == 0) {
+        const uint32_t idesc = make_idesc(128, N, FP8 ? 0u : 1u, false);
+        const uint64_t da = sdesc_sw128(smem_u32(a), 16, 1024);
+        const uint64_t db = sdesc_sw128(smem_u32(b), 16, 1024);
+        const unsigned long long t0 = clock64();
+#pragma unroll 1
+        for (int i = 0; i < iters; ++i) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                // k step: 32 bytes (16 bf16 / 32 e4m3 elements) along the 128-byte rows
+                const uint64_t off = (uint64_t)((kk * 32) >> 4);
+                if constexpr (FP8)
+                    umma_f8_ss(tmem, da + off, db + off, idesc, (i | kk) != 0);
+                else
+                    umma_f16_ss(tmem, da + off, db + off, idesc, (i | kk) != 0);
+            }
+        }
+        umma_commit(smem_u32(bar));
+        const unsigned long long g0 = globaltimer_ns();
+        bool ok = true;
+        while (!mbar_try_wait(smem_u32(bar), 0u)) {
+            if (globaltimer_ns() - g0 > limit_ns) {
+                ok = false;
+                break;
+            }
+        }
+        const unsigned long long t1 = clock64();
+        if (!ok) {
+            atomicOr(err, 1u);
+            // the MMAs still read shared memory and write TMEM: wait for them once more
+            const unsigned long long g1 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(bar), 0u) && globaltimer_ns() - g1 < limit_ns) {
+            }
+        }
+        cycles[blockIdx.x] = t1 - t0;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int N, bool FP8>
+cudaError_t launch_mma(int grid, int iters, unsigned long long* cycles, uint32_t* err,
+                       unsigned long long limit_ns, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(mb_mma_kernel<N, FP8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
+    if (e != cudaSuccess) return e;
+    mb_mma_kernel<N, FP8><<<grid, 128, kMmaSmem, s>>>(iters, cycles, err, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_mb_ex2(int grid, int iters, unsigned long long* cycles, float* sink, void* stream) {
+    if (grid < 1 || iters < 1 || !cycles || !sink) return (int)cudaErrorInvalidValue;
+    mb_ex2_kernel<<<grid, kEx2Threads, 0, static_cast<cudaStream_t>(stream)>>>(iters, cycles, sink);
+    return (int)cudaGetLastError();
+}
+
+long long fa_mb_ex2_per_cta(int iters) { return (long long)kEx2Threads * kEx2Chains * 4 * iters; }
+
+int fa_mb_mma(int grid, int n, int fp8, int iters, unsigned long long* cycles, uint32_t* err,
+              unsigned long long limit_ns, void* stream) {
+    if (grid < 1 || iters < 1 || !cycles || !err) return (int)cudaErrorInvalidValue;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!fp8 && n == 64) return (int)launch_mma<64, false>(grid, iters, cycles, err, limit_ns, s);
+    if (!fp8 && n == 128) return (int)launch_mma<128, false>(grid, iters, cycles, err, limit_ns, s);
+    if (!fp8 && n == 256) return (int)launch_mma<256, false>(grid, iters, cycles, err, limit_ns, s);
+    if (fp8 && n == 128) return (int)launch_mma<128, true>(grid, iters, cycles, err, limit_ns, s);
+    if (fp8 && n == 256) return (int)launch_mma<256, true>(grid, iters, cycles, err, limit_ns, s);
+    return (int)cudaErrorInvalidValue;
+}
+
+long long fa_mb_mma_flops_per_cta(int n, int fp8, int iters) {
+    // 4 MMAs per iteration (the 128-byte rows hold K = 64 bf16 or K = 128 e4m3), each
+    // 2 * M * N * K FLOPs with M = 128
+    const long long k_per_mma = fp8 ? 32 : 16;
+    return 4LL * iters * 2LL * 128 * n * k_per_mma;
+}
+
+}  // extern "C"

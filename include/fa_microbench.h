@@ -1,0 +1,60 @@
+/*
+ * fa_microbench.h -- C ABI of the throughput probes (_fa_microbench.so) that
+ * measure the two ceilings of the attention forward kernel on this GPU: the
+ * MUFU exponential rate and the tcgen05 tensor-pipe rate.
+ *
+ * Why: the page "Dissecting the SM_120 Microarchitecture" (section 11.2,
+ * Fig. 12) finds exp2 on the special-function unit, not the MMAs, to dominate
+ * a key block of fused attention on a GPU without Tensor Memory.  A forward
+ * pass computes one exp2 per visible (query row, key) pair and
+ * 4 * head_dim FLOPs per pair, so its attainable time is the larger of the
+ * two quotients; these probes supply both denominators, measured.
+ *
+ * All pointers are device pointers owned by the caller; all launches are
+ * asynchronous on `stream` (a cudaStream_t).  Every wait inside a kernel is
+ * bounded (limit_ns of %globaltimer); a wait that runs out sets *err != 0.
+ * The return value is a cudaError_t (0 = launched).
+ */
+#ifndef FA_MICROBENCH_H
+#define FA_MICROBENCH_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FA_MB_API __attribute__((visibility("default")))
+#else
+#define FA_MB_API
+#endif
+
+/*
+ * ex2.approx.ftz.f32 throughput.  `grid` CTAs of 1024 threads (one per SM),
+ * each thread `iters` x 32 exponentials in 8 independent chains.  Writes the
+ * SM cycles of each CTA to cycles[grid] (uint64); sink[1024] is never written
+ * in practice (it keeps the chains from being optimised away).
+ */
+FA_MB_API int fa_mb_ex2(int grid, int iters, unsigned long long* cycles, float* sink,
+                        void* stream);
+/* exponentials one CTA of fa_mb_ex2 evaluates */
+FA_MB_API long long fa_mb_ex2_per_cta(int iters);
+
+/*
+ * tcgen05.mma issue rate.  `grid` CTAs (one per SM); in each one thread
+ * issues 4 x `iters` MMAs of M = 128, N = n (64, 128 or 256 for bf16; 128 or
+ * 256 for e4m3) and K = 16 (bf16, kind::f16) or 32 (e4m3, kind::f8f6f4), A and
+ * B from shared memory, fp32 accumulate in Tensor Memory, then waits for their
+ * completion.  Writes each CTA's SM cycles to cycles[grid].
+ */
+FA_MB_API int fa_mb_mma(int grid, int n, int fp8, int iters, unsigned long long* cycles,
+                        uint32_t* err, unsigned long long limit_ns, void* stream);
+/* FLOPs one CTA of fa_mb_mma performs (2 * M * N * K per MMA) */
+FA_MB_API long long fa_mb_mma_flops_per_cta(int n, int fp8, int iters);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_MICROBENCH_H */

@@ -15,7 +15,7 @@ def test_exp2_bound_of_the_causal_8k_pass():
     # B=2, H=32, S=8192, D=128, causal: 4 B H S^2 D / 2 FLOPs and one exp2 per visible
     # (query row, key) pair, B H S^2 / 2
     flops = 4.0 * 2 * 32 * 8192 * 8192 * 128 / 2
-    r = bench.exp2_bound(flops, 128, 1928.9, 152, 2070.0)
+    r = bench.exp2_bound(flops, 128, 1928.9, 152, 2070.0, 32.0)
     assert math.isclose(r["exp2_per_launch"], 2 * 32 * 8192 * 8192 / 2)
     assert math.isclose(r["tensor_ms"], flops / 1928.9e12 * 1e3)
     assert math.isclose(r["exp2_ms"], 2 * 32 * 8192 * 8192 / 2 / (32 * 152 * 2070e6) * 1e3)
@@ -25,7 +25,7 @@ def test_exp2_bound_of_the_causal_8k_pass():
 
 def test_exp2_bound_picks_the_larger_time():
     # head dim 8: 16x fewer FLOPs per exp2 than at 128, so the MUFU limits
-    r = bench.exp2_bound(4.0 * 8 * 1e9, 8, 1928.9, 152, 2070.0)
+    r = bench.exp2_bound(4.0 * 8 * 1e9, 8, 1928.9, 152, 2070.0, 32.0)
     assert r["limit"] == "exp2" and r["attainable_ms"] == r["exp2_ms"] > r["tensor_ms"]
 
 
@@ -35,3 +35,8 @@ def test_flop_count_of_the_workloads():
     assert bench._flops(w, None) == 4.0 * 2 * 32 * 8192 * 8192 * 128 / 2
     w = inputs.WORKLOADS["bf16_noncausal_8k"]
     assert bench._flops(w, None) == 4.0 * 2 * 32 * 8192 * 8192 * 128
+
+
+def test_per_sm_rates():
+    r = bench._per_sm_rates(1000.0, [10, 20, 40, 0])
+    assert r == {"median": 50.0, "min": 25.0, "max": 100.0}
