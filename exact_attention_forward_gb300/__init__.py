@@ -44,7 +44,8 @@ EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_num_splits", "fa_
                     "fa_last_error_detail", "fa_device_error", "fa_debug_set",
                     "fa_fwd_static_workspace", "fa_fwd_gqa", "fa_fwd_fp8", "fa_fwd_kvcache",
                     "fa_fwd_workspace_size_gqa", "fa_fwd_num_splits_gqa", "fa_fwd_2cta",
-                    "fa_fwd_kvcache_workspace_size", "fa_fwd_kvcache_num_splits")
+                    "fa_fwd_kvcache_workspace_size", "fa_fwd_kvcache_num_splits",
+                    "fa_debug_trace", "fa_debug_trace_bytes")
 
 _lock = threading.Lock()
 _lib = None
@@ -92,6 +93,10 @@ def load_library():
         lib.fa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         lib.fa_debug_set.restype = None
         lib.fa_debug_set.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
+        lib.fa_debug_trace.restype = i32
+        lib.fa_debug_trace.argtypes = [vp, sz]
+        lib.fa_debug_trace_bytes.restype = sz
+        lib.fa_debug_trace_bytes.argtypes = []
         lib.fa_fwd_gqa.restype = i32
         lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, i32,
                                    i32, i32, f32, i32, i32, vp, vp, vp, vp, sz, vp]

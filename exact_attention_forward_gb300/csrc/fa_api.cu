@@ -20,8 +20,12 @@ namespace fa {
 __device__ uint32_t g_fa_error_word;
 
 // Work counters of the greedy item scheduler (varlen launches): one {next item, CTAs
-// done} pair per launch slot.  Each launch takes the next slot round-robin and its last CTA returns the
-// pair to zero, so up to kSchedSlots launches may be in flight on a device at once.
+// done} pair per launch slot.  Each launch takes the next slot of its range round-robin
+// (eager launches and launches captured into CUDA graphs have separate ranges) and its
+// last CTA returns the pair to zero, so up to 192 eager launches may be in flight on a
+// device at once.  A captured launch keeps its slot in every replay: two replays of one
+// graph, or of two graphs whose varlen launches drew the same captured slot (64 apart),
+// must not run at the same time.
 constexpr int kSchedSlots = 256;
 __device__ uint32_t g_fa_sched[2 * kSchedSlots];
 
@@ -34,11 +38,23 @@ thread_local char t_detail[512] = "";
 std::mutex g_mu;
 uint64_t g_wait_limit_ns = kDefaultWaitNs;
 uint32_t g_inject = 0;
+uint64_t* g_trace = nullptr;  // event log of a FA_TRACE build (fa_debug_trace)
 int g_num_sms[kMaxDevices] = {0};
+// Device addresses of the library's __device__ variables, valid for the context they were
+// looked up in: a cudaDeviceReset (or any new context) reloads the module at other
+// addresses, so they are looked up again whenever the current context's id changes.
+unsigned long long g_addr_ctx[kMaxDevices] = {0};
 uint32_t* g_err_addr[kMaxDevices] = {nullptr};
 uint32_t* g_sched_addr[kMaxDevices] = {nullptr};
+// Counter slots: eager launches take [0, kEagerSlots) round-robin; launches recorded into
+// a CUDA graph keep their slot for every replay, so they take theirs from the separate
+// range [kEagerSlots, kSchedSlots) and never share one with an eager launch.
+constexpr int kEagerSlots = 192;
 std::atomic<uint32_t> g_sched_next{0};
+std::atomic<uint32_t> g_sched_next_captured{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_get_id = nullptr;
 
 fa_status fail(fa_status s, const char* fmt, ...) {
     va_list ap;
@@ -50,15 +66,56 @@ fa_status fail(fa_status s, const char* fmt, ...) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Driver entry points, resolved once (g_mu held).
+bool driver_entry(const char* name, int version, void** fn) {
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion(name, fn, version, cudaEnableDefault, &q);
+    return e == cudaSuccess && q == cudaDriverEntryPointSuccess && *fn;
+}
+
+// Unique id of the calling thread's current context, 0 if there is none yet (g_mu held).
+unsigned long long context_id_locked() {
+    if (!g_ctx_current || !g_ctx_get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+fa_status resolve_driver_entries() {
+    if (!g_encode) {
+        void* fn = nullptr;
+        if (!driver_entry("cuTensorMapEncodeTiled", 12000, &fn))
+            return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (!g_ctx_current || !g_ctx_get_id) {
+        void *f1 = nullptr, *f2 = nullptr;
+        if (!driver_entry("cuCtxGetCurrent", 4000, &f1) || !driver_entry("cuCtxGetId", 12000, &f2))
+            return fail(FA_ERR_CUDA, "cuCtxGetCurrent / cuCtxGetId entry points unavailable");
+        g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f1);
+        g_ctx_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f2);
+    }
+    return FA_OK;
+}
+
 fa_status device_info(int* dev, int* sms, uint32_t** err) {
     cudaError_t e = cudaGetDevice(dev);
     if (e != cudaSuccess) return fail(FA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (*dev < 0 || *dev >= kMaxDevices) return fail(FA_ERR_CUDA, "device index %d out of range", *dev);
     std::lock_guard<std::mutex> lk(g_mu);
+    fa_status st = resolve_driver_entries();
+    if (st != FA_OK) return st;
     if (g_num_sms[*dev] == 0) {
         int n = 0;
         e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, *dev);
         if (e != cudaSuccess) return fail(FA_ERR_CUDA, "SM count: %s", cudaGetErrorString(e));
+        g_num_sms[*dev] = n;
+    }
+    const unsigned long long ctx = context_id_locked();
+    if (ctx == 0 || ctx != g_addr_ctx[*dev]) {
+        // (the lookup also creates the device's primary context if nothing has yet)
         void* addr = nullptr;
         e = cudaGetSymbolAddress(&addr, g_fa_error_word);
         if (e != cudaSuccess) return fail(FA_ERR_CUDA, "error word: %s", cudaGetErrorString(e));
@@ -66,23 +123,22 @@ fa_status device_info(int* dev, int* sms, uint32_t** err) {
         e = cudaGetSymbolAddress(&addr, g_fa_sched);
         if (e != cudaSuccess) return fail(FA_ERR_CUDA, "work counters: %s", cudaGetErrorString(e));
         g_sched_addr[*dev] = static_cast<uint32_t*>(addr);
-        g_num_sms[*dev] = n;
-    }
-    if (!g_encode) {
-        cudaDriverEntryPointQueryResult q;
-        void* fn = nullptr;
-        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
-            return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
-        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        g_addr_ctx[*dev] = context_id_locked();
     }
     *sms = g_num_sms[*dev];
     *err = g_err_addr[*dev];
     return FA_OK;
 }
 
-uint32_t* next_sched_slot(int dev) {
-    const uint32_t slot = g_sched_next.fetch_add(1u) % (uint32_t)kSchedSlots;
+uint32_t* next_sched_slot(int dev, cudaStream_t s) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    const bool captured = cudaStreamIsCapturing(s, &cap) == cudaSuccess &&
+                          cap == cudaStreamCaptureStatusActive;
+    const uint32_t slot =
+        captured ? (uint32_t)kEagerSlots +
+                       g_sched_next_captured.fetch_add(1u) % (uint32_t)(kSchedSlots - kEagerSlots)
+                 : g_sched_next.fetch_add(1u) % (uint32_t)kEagerSlots;
+    std::lock_guard<std::mutex> lk(g_mu);
     return g_sched_addr[dev] + 2 * slot;
 }
 
@@ -469,7 +525,7 @@ fa_status fwd_impl(const FwdArgs& a) {
     p.seqused_k = a.seqused_k;
     p.seqused_add = a.seqused_add;
     p.err = err;
-    p.sched = next_sched_slot(dev);
+    p.sched = next_sched_slot(dev, static_cast<cudaStream_t>(a.stream));
     p.batch = a.batch;
     p.heads = a.heads;
     p.kv_group = a.heads / a.heads_k;
@@ -505,6 +561,7 @@ fa_status fwd_impl(const FwdArgs& a) {
         std::lock_guard<std::mutex> lk(g_mu);
         p.wait_limit_ns = g_wait_limit_ns;
         p.inject = g_inject;
+        p.trace = g_trace;
     }
 
     // ---------------------------------------------------------------- tensor maps
@@ -581,6 +638,12 @@ fa_status fwd_impl(const FwdArgs& a) {
 
 fa_status set_error_detail(fa_status status, const char* msg) { return fail(status, "%s", msg); }
 
+unsigned long long current_context_id() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (resolve_driver_entries() != FA_OK) return 0;
+    return context_id_locked();
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -607,6 +670,22 @@ void fa_debug_set(uint64_t wait_limit_ns, uint32_t inject) {
     g_wait_limit_ns = wait_limit_ns ? wait_limit_ns : kDefaultWaitNs;
     g_inject = inject;
 }
+
+fa_status fa_debug_trace(void* buf, size_t bytes) {
+#ifdef FA_TRACE
+    if (buf && (bytes < kTraceBytes || !aligned16(buf)))
+        return fail(FA_ERR_INVALID_ARG, "trace buffer needs %zu bytes, 16-byte aligned", kTraceBytes);
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_trace = static_cast<uint64_t*>(buf);
+    return FA_OK;
+#else
+    (void)buf;
+    (void)bytes;
+    return fail(FA_ERR_UNSUPPORTED, "this library was built without FA_TRACE");
+#endif
+}
+
+size_t fa_debug_trace_bytes(void) { return kTraceBytes; }
 
 fa_status fa_device_error(uint32_t* flags, int clear) {
     int dev, sms;

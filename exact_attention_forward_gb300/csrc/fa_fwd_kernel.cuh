@@ -123,6 +123,32 @@ constexpr float kExp2C2 = 0.2426113784313202f;
 constexpr float kExp2C3 = 0.05517187342047691f;
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + magic rounds x to an integer
 
+// Optional event trace (built with -DFA_TRACE; without it every hook below compiles to
+// nothing).  The first kTraceCtas CTAs log (tag << 56 | clock64) words per role -- 0 the
+// producer, 1 the MMA issuer, 2 + t the first thread of tile t's softmax warps -- into
+// p.trace[(cta * 4 + role) * kTraceCap + i], up to kTraceCap events each.  Tags:
+//   producer: 1 item start, 2 + t Q_EMPTY[t] passed, 4 K/V group issued, 5 next item published
+//   issuer:   1 item read, 2 Q ready, 3 K/V group ready, 4 + t P[t] ready, 6 + t tile t's
+//             MMAs of a block issued, 8 item done
+//   softmax:  1 item read, 2 S ready, 3 P handed over, 4 O ready, 5 O released (TMEM),
+//             6 epilogue done
+struct Tracer {
+#ifdef FA_TRACE
+    uint64_t* buf = nullptr;
+    uint32_t n = 0;
+    __device__ __forceinline__ void init(uint64_t* base, int role) {
+        buf = (base && blockIdx.x < kTraceCtas) ? base + ((size_t)blockIdx.x * 4 + role) * kTraceCap
+                                               : nullptr;
+    }
+    __device__ __forceinline__ void ev(uint32_t tag) {
+        if (buf && n < (uint32_t)kTraceCap) buf[n++] = ((uint64_t)tag << 56) | (clock64() & 0xFFFFFFFFFFFFFFull);
+    }
+#else
+    __device__ __forceinline__ void init(uint64_t*, int) {}
+    __device__ __forceinline__ void ev(uint32_t) {}
+#endif
+};
+
 // Register split: launched at 168 per thread (384 x 168 = 64512); the producer /
 // MMA warpgroup gives up 64 per thread, the two softmax warpgroups take 32 more.
 constexpr uint32_t kRegsLoadMma = 104;
@@ -373,7 +399,7 @@ __device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, 
 enum : uint32_t {
     SITE_Q_EMPTY = 1, SITE_KV_EMPTY = 2, SITE_Q_FULL = 3, SITE_KV_FULL = 4, SITE_P_FULL = 5,
     SITE_O_EMPTY = 6, SITE_S_FULL = 7, SITE_O_FULL = 8, SITE_DRAIN = 9, SITE_STG_FULL = 10,
-    SITE_STG_EMPTY = 11, SITE_ITEM_FULL = 12, SITE_ITEM_EMPTY = 13
+    SITE_STG_EMPTY = 11, SITE_ITEM_FULL = 12, SITE_ITEM_EMPTY = 13, SITE_LOAD_DRAIN = 14
 };
 
 template <int D, bool FP8, bool PAIR = false>
@@ -477,7 +503,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("griddepcontrol.wait;" ::: "memory");
             const uint64_t pol_q = l2_policy_evict_first();
             const uint64_t pol_kv = l2_policy_evict_last();
+            Tracer tr;
+            tr.init(p.trace, 0);
             uint32_t ring = 0, ph_qe = 0;  // bit t: parity of the last Q_EMPTY wait of tile t
+            // loads in flight: bit t / s toggles whenever Q_FULL[t] / KV_FULL[s] is armed
+            // (its phase parity), and stays set in the *_any masks once it has been armed
+            uint32_t q_par = 0, q_any = 0, kv_par = 0, kv_any = 0;
             bool withheld = false;
             bool aborted = false;
             uint32_t published = 0;
@@ -598,6 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the next index is requested now and published once this item's loads have
                 // been issued, so the counter's round trip overlaps them
                 ++round_no;
+                tr.ev(1);
                 const uint32_t ticket = greedy ? atomicAdd(p.sched, 1u) : 0u;
                 const Item it = it_next;
                 const int bc = p.varlen ? 0 : it.b;  // batch coordinate of the 4-D view
@@ -606,6 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (it.n_hi_t[t] <= it.n_lo) return true;
                     if (!wait_bar(bar(C::Q_EMPTY + t), ((ph_qe >> t) & 1u) ^ 1u, wc, SITE_Q_EMPTY))
                         return false;
+                    tr.ev(2 + t);
                     ph_qe ^= 1u << t;
                     if (p.inject == 1u && !withheld) {  // debug: never arrive on this Q tile
                         withheld = true;
@@ -614,7 +647,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // packed mode: the map's box spans G heads x 128/G rows
                     const int qrow = (p.varlen ? it.q_row0 : 0) + it.m0[t] / p.pack;
                     // a pair's Q tiles both land on the even CTA's barrier, which expects them
-                    if (rank == 0u) mbar_arrive_expect_tx(bar(C::Q_FULL + t), (PAIR ? 2 : 1) * C::kTileBytes);
+                    if (rank == 0u) {
+                        mbar_arrive_expect_tx(bar(C::Q_FULL + t), (PAIR ? 2 : 1) * C::kTileBytes);
+                        q_par ^= 1u << t;
+                        q_any |= 1u << t;
+                    }
 #pragma unroll
                     for (int c = 0; c < C::kChunks; ++c) {
                         if constexpr (PAIR)
@@ -668,8 +705,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 };
                 // bytes a group of n slots brings to its barrier (both CTAs' halves in a pair;
                 // only the even CTA, which owns the barrier, announces them)
-                auto expect_group = [&](uint32_t full, uint32_t n) {
-                    if (rank == 0u) mbar_arrive_expect_tx(full, n * (PAIR ? 2u : 1u) * C::kSlotBytes);
+                auto expect_group = [&](uint32_t slot, uint32_t n) {
+                    if (rank == 0u) {
+                        mbar_arrive_expect_tx(bar(C::KV_FULL + slot), n * (PAIR ? 2u : 1u) * C::kSlotBytes);
+                        kv_par ^= 1u << slot;
+                        kv_any |= 1u << slot;
+                    }
                 };
                 // Few new cache rows (decoding): the ones inside this item's key blocks go
                 // into the caches now, before any of those blocks is loaded -- generic-proxy
@@ -708,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     uint32_t full = bar(C::KV_FULL + ring % C::kStages);
-                    expect_group(full, 1u);
+                    expect_group(ring % C::kStages, 1u);
                     load_kv(ring, false, j0, full);
                     ++ring;
                     for (int j = j0; j >= it.n_lo; --j) {
@@ -718,10 +759,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         full = bar(C::KV_FULL + ring % C::kStages);
-                        expect_group(full, pair ? 2u : 1u);
+                        expect_group(ring % C::kStages, pair ? 2u : 1u);
                         load_kv(ring, true, j, full);
                         if (pair) load_kv(ring + 1, false, j - 1, full);
                         ring += pair ? 2u : 1u;
+                        tr.ev(4);
                     }
                 }
                 if (aborted) break;
@@ -737,11 +779,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     aborted = true;
                     break;
                 }
+                tr.ev(5);
             }
             if (greedy) fetching_done();  // after an abort, or with no item beyond the first
-            if (aborted) {  // let copies already in flight land before the CTA retires
-                const uint64_t t0 = globaltimer_ns();
-                while (globaltimer_ns() - t0 < 200000ull) {
+            if (aborted) {
+                // Loads already issued must land before the CTA retires (its shared memory
+                // may go to the next CTA on this SM): wait, bounded and regardless of the
+                // abort flag, for the last armed phase of every full barrier -- phases of one
+                // barrier complete in order, so that covers every earlier load too.
+#pragma unroll 1
+                for (int t = 0; t < kTiles; ++t)
+                    if ((q_any >> t) & 1u)
+                        wait_slow(bar(C::Q_FULL + t), ((q_par >> t) & 1u) ^ 1u, wc, SITE_LOAD_DRAIN, false);
+#pragma unroll 1
+                for (int s = 0; s < C::kStages; ++s)
+                    if ((kv_any >> s) & 1u)
+                        wait_slow(bar(C::KV_FULL + s), ((kv_par >> s) & 1u) ^ 1u, wc, SITE_LOAD_DRAIN, false);
+                if constexpr (PAIR) {
+                    // the odd CTA's halves complete on the even CTA's barriers, which it
+                    // cannot watch, and it may have run ahead of the arming: a grace period
+                    const uint64_t t0 = globaltimer_ns();
+                    while (globaltimer_ns() - t0 < 200000ull) {
+                    }
                 }
             }
         }
@@ -789,6 +848,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto desc = [&](uint32_t lo) -> uint64_t { return ((uint64_t)d_hi << 32) | lo; };
             uint32_t ring = 0;
             uint32_t ph_q = 0, ph_p = 0, ph_o = 0;  // bit t: parity of the next wait on tile t
+            Tracer tr;
+            tr.init(p.trace, 1);
             uint32_t ph_kv = 0;  // bit s: parity of the next wait on KV_FULL[s] (armed per group)
             auto wait_kv = [&](uint32_t slot) -> bool {
                 if (!wait_bar(bar(C::KV_FULL + slot), (ph_kv >> slot) & 1u, wc, SITE_KV_FULL)) return false;
@@ -848,11 +909,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(bar(C::ITEM_EMPTY + ((items_read - 1) & 1u)));
                 if (w >= p.n_items) break;
                 if (it.n_hi <= it.n_lo) continue;
+                tr.ev(1);
                 const int hi0 = it.n_hi_t[0], hi1 = it.n_hi_t[1], lo = it.n_lo;
                 const bool has0 = hi0 > lo, has1 = hi1 > lo;
                 if (has0 && !wait_bar(bar(C::Q_FULL + 0), ph_q & 1u, wc, SITE_Q_FULL)) break;
                 if (has1 && !wait_bar(bar(C::Q_FULL + 1), (ph_q >> 1) & 1u, wc, SITE_Q_FULL)) break;
                 tc_fence_after();
+                tr.ev(2);
                 uint32_t acc0 = 0u, acc1 = 0u;  // becomes 1 after the tile's first PV
                 const int j0 = it.n_hi - 1;
                 const uint32_t kslot0 = ring % C::kStages;
@@ -881,6 +944,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         aborted = true;
                         break;
                     }
+                    tr.ev(3);
                     ++ring;
                     // a tile that does not visit block j releases V(j) at once (its load has
                     // landed, so the arrival belongs to this phase of the slot)
@@ -896,6 +960,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const bool nxt = has_next && (j - 1) < hi;
                         if (cur) {
                             if (!wait_handoff(bar(C::P_FULL + t), (ph_p >> t) & 1u, SITE_P_FULL)) return false;
+                            tr.ev(4 + t);
                             ph_p ^= 1u << t;
                             if (acc == 0u &&
                                 !wait_handoff(bar(C::O_EMPTY + t), ((ph_o >> t) & 1u) ^ 1u, SITE_O_EMPTY))
@@ -911,6 +976,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else if (cur) {
                             commit(bar(C::O_FULL + t));  // last block of tile t
                         }
+                        tr.ev(6 + t);
                         return true;
                     };
                     if (!tile_step(std::integral_constant<int, 0>{}, hi0, acc0) ||
@@ -924,6 +990,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (aborted) break;
+                tr.ev(8);
                 if (!FP8 && has0) commit(bar(C::Q_EMPTY + 0));
                 if (!FP8 && has1) commit(bar(C::Q_EMPTY + 1));
                 ph_q ^= (has0 ? 1u : 0u) | (has1 ? 2u : 0u);
@@ -955,6 +1022,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool aborted = false;
         uint32_t held = 0;  // 1 + the item-ring slot whose record this warp still reads (0: none)
         bool stg_owed = false;  // (thread 0 of the tile) its last O store's read is unconfirmed
+        Tracer tr;
+        tr.init(r_in_tile == 0 ? p.trace : nullptr, 2 + t);
         // output addresses of this thread's row of a tile starting at (packed) row m0 of the
         // item (b, h, split, first packed row q_row0); false past the sequence end
         auto out_addr = [&](int b, int h, int split, int q_row0, int sq, int m0, float*& lse_ptr,
@@ -1003,6 +1072,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0 && held) mbar_arrive(bar(C::ITEM_EMPTY + (held - 1u)));
             held = 1u + ((items_read - 1) & 1u);
             if (w >= p.n_items) break;
+            tr.ev(1);
             if (it.bad_len && r_in_tile == 0 && t == 0) atomicOr(p.err, kErrBadLength);
             const uint32_t item_base = kv_base;
             if (it.n_hi > it.n_lo) kv_base += 2u * (uint32_t)(it.n_hi - it.n_lo);
@@ -1062,6 +1132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++s_cnt;
                 tc_fence_after();
+                tr.ev(2);
                 // S_t(j) is complete: K(j) is consumed, and so is V(j+1) (PV_t(j+1) was issued
                 // before S_t(j) by the same thread, and MMAs complete in issue order)
                 if (releaser) {
@@ -1195,6 +1266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     else
                         mbar_arrive(bar(C::P_FULL + t));
                 }
+                tr.ev(3);
             }
             if (aborted) break;
             // ---------------- epilogue: O = O_acc / l, LSE = ln2 * (m + log2 l)
@@ -1208,6 +1280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++o_cnt;
             }
             tc_fence_after();
+            tr.ev(4);
             if (releaser) mbar_arrive(bar(C::KV_EMPTY + v_slot(it.n_lo)));  // PV_t(n_lo) is complete
             const bool has_mass = l_run > 0.0f;
             const float inv_l = has_mass ? o_scale / l_run : 0.0f;
@@ -1254,6 +1327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     else
                         mbar_arrive(bar(C::O_EMPTY + t));
                 }
+                tr.ev(5);
                 // the last store of the previous epilogue out of this buffer: its issuing
                 // thread confirms that the TMA engine has read it only now, when the buffer is
                 // needed again, instead of waiting for it at the end of that epilogue
@@ -1343,6 +1417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *lse_ptr = has_mass ? (m_run + lg2_approx(l_run)) * 0.69314718055994531f : -INFINITY;
                 if (p.split) mark_empty_slots(lse_ptr, io.fill);
             }
+            tr.ev(6);
         }
     }
 
@@ -1375,17 +1450,19 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
                        const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t stream,
                        bool after_append) {
     using C = Cfg<D, FP8, PAIR>;
-    // The shared-memory attribute is set once per device (devices 0-63; others every
-    // launch): an atomic flag per device, so concurrent host threads at worst set it twice.
-    static std::atomic<bool> attr_done[64];
+    // The shared-memory attribute is set once per device and context (devices 0-63; others
+    // every launch): the context id it was set in is kept per device, so a new context
+    // (after cudaDeviceReset) sets it again; concurrent host threads at worst set it twice.
+    static std::atomic<unsigned long long> attr_ctx[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_acquire)) {
+    const unsigned long long ctx = current_context_id();
+    if (dev < 0 || dev >= 64 || ctx == 0 || attr_ctx[dev].load(std::memory_order_acquire) != ctx) {
         e = cudaFuncSetAttribute(fa_fwd_kernel<D, FP8, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
+        if (dev >= 0 && dev < 64) attr_ctx[dev].store(ctx, std::memory_order_release);
     }
     if (!after_append && !PAIR) {
         fa_fwd_kernel<D, FP8, PAIR><<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, o, p);

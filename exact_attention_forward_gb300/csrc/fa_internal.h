@@ -63,9 +63,16 @@ struct FwdParams {
     int v_e5m2;                 // FP8: V stored as E5M2 (Q, K and P stay E4M3)
     uint64_t wait_limit_ns;     // bound of every device-side wait
     uint32_t inject;            // debug fault injection (see fa_debug_set)
+    uint64_t* trace;            // event log of a build with FA_TRACE (see fa_debug_trace), or null
 };
 
 enum : uint32_t { kErrTimeout = 1u, kErrBadLength = 2u };
+
+// Event trace of a build with -DFA_TRACE: CTAs [0, kTraceCtas) log up to kTraceCap events
+// per role (4 roles) as 64-bit words (fa_debug_trace).
+constexpr int kTraceCtas = 8;
+constexpr int kTraceCap = 8192;
+constexpr size_t kTraceBytes = (size_t)kTraceCtas * 4 * kTraceCap * sizeof(uint64_t);
 
 // Kernel instances (one translation unit each).
 // q, k, v: TMA load maps; o: TMA store map of the bf16 output (same 4-D view as q);
@@ -91,9 +98,13 @@ cudaError_t launch_append_kv(void* k_cache, void* v_cache, const void* k_new, co
 cudaError_t launch_combine(const float* ws_o, const float* ws_lse, void* o, float* lse,
                            int batch, int heads, int seqlen_q, int dv, int n_splits,
                            cudaStream_t s);
-uint32_t* device_error_word();  // address of the device error word (current device)
 // Records `msg` as this thread's fa_last_error_detail() and returns `status` (for entry
 // points outside fa_api.cu).
 fa_status set_error_detail(fa_status status, const char* msg);
+// Unique id (cuCtxGetId) of the calling thread's current CUDA context, 0 if none.  Device
+// addresses of __device__ variables and per-function attributes belong to one context;
+// state cached per device is keyed on this so that a new context (after cudaDeviceReset)
+// sets it up again.
+unsigned long long current_context_id();
 
 }  // namespace fa

@@ -21,7 +21,9 @@
 //    array and corrupt each other's results; serialise them.
 //  * the first call on a device looks up the array's device address
 //    (cudaGetSymbolAddress, with that device current); make that first call
-//    before any stream capture.
+//    before any stream capture.  The address belongs to the device's current
+//    context: after a cudaDeviceReset the next call looks it up again (also
+//    before any capture).
 // No cudaMalloc, cudaFree or allocating library routine is called here.
 #include <mutex>
 
@@ -39,6 +41,7 @@ static __device__ __align__(256) unsigned char g_fa_static_scratch[kStaticScratc
 
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxDevices] = {0};  // context the address was looked up in
 
 }  // namespace
 
@@ -52,14 +55,16 @@ extern "C" fa_status fa_fwd_static_workspace(
         return fa::set_error_detail(FA_ERR_CUDA, "no usable current CUDA device");
     void* scratch = nullptr;
     {
+        const unsigned long long ctx = fa::current_context_id();
         std::lock_guard<std::mutex> lk(g_mu);
-        if (!g_scratch_addr[dev]) {
+        if (!g_scratch_addr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
             void* addr = nullptr;
             cudaError_t e = cudaGetSymbolAddress(&addr, g_fa_static_scratch);
             if (e != cudaSuccess || addr == nullptr)
                 return fa::set_error_detail(FA_ERR_CUDA,
                                             "device address of the static scratch unavailable");
             g_scratch_addr[dev] = addr;
+            g_scratch_ctx[dev] = fa::current_context_id();
         }
         scratch = g_scratch_addr[dev];
     }

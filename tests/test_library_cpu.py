@@ -193,3 +193,26 @@ def test_static_workspace_without_a_device_says_why(lib):
     assert st == fa.FA_ERR_CUDA
     detail = lib.fa_last_error_detail()
     assert b"no usable current CUDA device" in detail or b"static scratch" in detail, detail
+
+
+def test_microbench_library_exports_its_header():
+    text = open(os.path.join(ROOT, "include", "fa_microbench.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = sorted(set(re.findall(r"\b(fa_mb_[a-z0-9_]+)\s*\(", text)))
+    assert names == ["fa_mb_ex2", "fa_mb_ex2_per_cta", "fa_mb_mma", "fa_mb_mma_flops_per_cta"]
+    mb = ctypes.CDLL(_build.build_microbench())
+    for name in names:
+        assert isinstance(getattr(mb, name), ctypes._CFuncPtr)
+    mb.fa_mb_mma_flops_per_cta.restype = ctypes.c_longlong
+    mb.fa_mb_ex2_per_cta.restype = ctypes.c_longlong
+    # 4 MMAs of 2 * 128 * N * K per iteration; 1024 threads x 8 chains x 4 per iteration
+    assert mb.fa_mb_mma_flops_per_cta(256, 0, 10) == 4 * 10 * 2 * 128 * 256 * 16
+    assert mb.fa_mb_mma_flops_per_cta(128, 1, 10) == 4 * 10 * 2 * 128 * 128 * 32
+    assert mb.fa_mb_ex2_per_cta(10) == 1024 * 8 * 4 * 10
+
+
+def test_trace_is_unsupported_in_the_default_build(lib):
+    # the default library holds no trace code: asking for a trace says so
+    assert lib.fa_debug_trace(None, 0) == fa.FA_ERR_UNSUPPORTED
+    assert b"FA_TRACE" in lib.fa_last_error_detail()
+    assert lib.fa_debug_trace_bytes() == 8 * 4 * 8192 * 8
