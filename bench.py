@@ -20,6 +20,7 @@ slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -114,7 +115,8 @@ def measure_ex2_rate(dev, iters: int = 2048) -> dict:
 
 
 def measure_mma_rate(dev, n: int, fp8: bool, iters: int = 2048) -> dict:
-    """tcgen05.mma FLOP per SM clock, M = 128, N = n, one issuing thread per SM."""
+    """tcgen05.mma FLOP per SM clock, M = 128, N = n, one issuing thread per SM (n = -128:
+    N = 128 in the PV form, A from Tensor Memory and B MN-major)."""
     import torch
     lib = _microbench_lib()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -132,6 +134,32 @@ def measure_mma_rate(dev, n: int, fp8: bool, iters: int = 2048) -> dict:
     return _per_sm_rates(lib.fa_mb_mma_flops_per_cta(n, int(fp8), iters), cyc.cpu().tolist())
 
 
+def measure_load_rate(dev, window: int, iters: int = 4096) -> dict:
+    """cp.async.bulk bytes per SM clock into shared memory, each CTA (one per SM) reading its
+    own `window` bytes cyclically (after a first untimed pass)."""
+    import torch
+    lib = _microbench_lib()
+    lib.fa_mb_load.restype = ctypes.c_int
+    lib.fa_mb_load.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_int,
+                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_void_p]
+    lib.fa_mb_load_bytes_per_cta.restype = ctypes.c_longlong
+    lib.fa_mb_load_bytes_per_cta.argtypes = [ctypes.c_int]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    src = torch.ones(sms * window, dtype=torch.uint8, device=dev)
+    cyc = torch.zeros(sms, dtype=torch.int64, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    for _ in range(2):
+        rc = lib.fa_mb_load(sms, src.data_ptr(), window, iters, cyc.data_ptr(), err.data_ptr(),
+                            2_000_000_000, stream)
+        if rc != 0:
+            raise RuntimeError(f"fa_mb_load launch failed ({rc})")
+    torch.cuda.synchronize(dev)
+    if int(err.item()) != 0:
+        raise RuntimeError("fa_mb_load: a bounded wait ran out")
+    return _per_sm_rates(lib.fa_mb_load_bytes_per_cta(iters), cyc.cpu().tolist())
+
+
 def run_microbench(args):
     """One JSON line: ex2 and tcgen05 rates per SM clock, and what they give at the SM
     clock sampled while they ran."""
@@ -145,9 +173,15 @@ def run_microbench(args):
     mma = {}
     for n, fp8 in ((64, False), (128, False), (256, False), (128, True), (256, True)):
         mma[f"{'e4m3' if fp8 else 'bf16'}_m128_n{n}"] = measure_mma_rate(dev, n, fp8)
+    for fp8 in (False, True):  # the PV form: A from Tensor Memory, B MN-major
+        mma[f"{'e4m3' if fp8 else 'bf16'}_m128_n128_a_tmem_b_mn_major"] = measure_mma_rate(dev, -128, fp8)
+    loads = {"l2_window_256KiB": measure_load_rate(dev, 256 << 10),
+             "hbm_window_32MiB": measure_load_rate(dev, 32 << 20, iters=2048)}
     clocks = sampler.stop()
     mhz = clocks.get("sm_mhz") or 2070.0
-    line = {"microbench": "ex2 / tcgen05 throughput", "sms": sms, "clocks": clocks,
+    line = {"microbench": "ex2 / tcgen05 / bulk-copy throughput", "sms": sms, "clocks": clocks,
+            "load_bytes_per_clk_per_sm": loads,
+            "load_gbs_chip_at_sm_mhz": {k: v["median"] * sms * mhz * 1e6 / 1e9 for k, v in loads.items()},
             "ex2_per_clk_per_sm": ex2,
             "ex2_per_s_chip_at_sm_mhz": ex2["median"] * sms * mhz * 1e6,
             "mma_flop_per_clk_per_sm": mma,

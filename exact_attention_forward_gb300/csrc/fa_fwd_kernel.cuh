@@ -124,27 +124,41 @@ constexpr float kExp2C3 = 0.05517187342047691f;
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + magic rounds x to an integer
 
 // Optional event trace (built with -DFA_TRACE; without it every hook below compiles to
-// nothing).  The first kTraceCtas CTAs log (tag << 56 | clock64) words per role -- 0 the
-// producer, 1 the MMA issuer, 2 + t the first thread of tile t's softmax warps -- into
-// p.trace[(cta * 4 + role) * kTraceCap + i], up to kTraceCap events each.  Tags:
+// nothing).  kTraceCtas CTAs spread over the grid (slot k: CTA k * (grid - 1) /
+// (kTraceCtas - 1)) log (tag << 56 | clock64) words per role -- 0 the producer, 1 the MMA
+// issuer, 2 + t the first thread of tile t's softmax warps -- into
+// p.trace[(slot * kTraceRoles + role) * kTraceCap + i], up to kTraceCap events each.  Tags:
 //   producer: 1 item start, 2 + t Q_EMPTY[t] passed, 4 K/V group issued, 5 next item published
 //   issuer:   1 item read, 2 Q ready, 3 K/V group ready, 4 + t P[t] ready, 6 + t tile t's
 //             MMAs of a block issued, 8 item done
 //   softmax:  1 item read, 2 S ready, 3 P handed over, 4 O ready, 5 O released (TMEM),
 //             6 epilogue done
+//   every role, first and last: 15 %globaltimer (ns), then 14 clock64 -- ties the SM's
+//   cycle count to wall time across SMs
 struct Tracer {
 #ifdef FA_TRACE
     uint64_t* buf = nullptr;
     uint32_t n = 0;
     __device__ __forceinline__ void init(uint64_t* base, int role) {
-        buf = (base && blockIdx.x < kTraceCtas) ? base + ((size_t)blockIdx.x * 4 + role) * kTraceCap
-                                               : nullptr;
+        // traced CTAs spread over the grid: slot k is CTA k * (grid - 1) / (kTraceCtas - 1)
+        const int g1 = (int)gridDim.x - 1, c = (int)blockIdx.x;
+        const int k = g1 > 0 ? (c * (kTraceCtas - 1) + g1 / 2) / g1 : 0;
+        const bool on = base && k < kTraceCtas && (g1 > 0 ? k * g1 / (kTraceCtas - 1) : 0) == c;
+        buf = on ? base + ((size_t)k * kTraceRoles + role) * kTraceCap : nullptr;
+        fin();
+    }
+    __device__ __forceinline__ void fin() {
+        if (buf && n + 2 <= (uint32_t)kTraceCap) {
+            buf[n++] = (15ull << 56) | (globaltimer_ns() & 0xFFFFFFFFFFFFFFull);
+            buf[n++] = (14ull << 56) | (clock64() & 0xFFFFFFFFFFFFFFull);
+        }
     }
     __device__ __forceinline__ void ev(uint32_t tag) {
         if (buf && n < (uint32_t)kTraceCap) buf[n++] = ((uint64_t)tag << 56) | (clock64() & 0xFFFFFFFFFFFFFFull);
     }
 #else
     __device__ __forceinline__ void init(uint64_t*, int) {}
+    __device__ __forceinline__ void fin() {}
     __device__ __forceinline__ void ev(uint32_t) {}
 #endif
 };
@@ -782,6 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tr.ev(5);
             }
             if (greedy) fetching_done();  // after an abort, or with no item beyond the first
+            tr.fin();
             if (aborted) {
                 // Loads already issued must land before the CTA retires (its shared memory
                 // may go to the next CTA on this SM): wait, bounded and regardless of the
@@ -1003,6 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
                 umma_commit(bar(C::DRAIN));
             if (!mbar_try_wait(bar(C::DRAIN), 0u)) wait_slow(bar(C::DRAIN), 0u, wc, SITE_DRAIN, false);
+            tr.fin();
         }
         __syncwarp();
     }
@@ -1419,6 +1435,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tr.ev(6);
         }
+#ifdef FA_TRACE
+        if (r_in_tile == 0) bulk_wait_group0();  // (the trace's end: the tile's stores done)
+#endif
+        tr.fin();
     }
 
     // the TMA stores of O have completed before this CTA retires (their issuing threads wait)

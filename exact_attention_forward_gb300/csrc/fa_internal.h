@@ -68,11 +68,12 @@ struct FwdParams {
 
 enum : uint32_t { kErrTimeout = 1u, kErrBadLength = 2u };
 
-// Event trace of a build with -DFA_TRACE: CTAs [0, kTraceCtas) log up to kTraceCap events
-// per role (4 roles) as 64-bit words (fa_debug_trace).
+// Event trace of a build with -DFA_TRACE: kTraceCtas CTAs log up to kTraceCap events per
+// role (kTraceRoles roles) as 64-bit words (fa_debug_trace).
 constexpr int kTraceCtas = 8;
+constexpr int kTraceRoles = 4;
 constexpr int kTraceCap = 8192;
-constexpr size_t kTraceBytes = (size_t)kTraceCtas * 4 * kTraceCap * sizeof(uint64_t);
+constexpr size_t kTraceBytes = (size_t)kTraceCtas * kTraceRoles * kTraceCap * sizeof(uint64_t);
 
 // Kernel instances (one translation unit each).
 // q, k, v: TMA load maps; o: TMA store map of the bf16 output (same 4-D view as q);

@@ -56,14 +56,19 @@ __global__ void __launch_bounds__(kEx2Threads, 1)
 
 constexpr int kMmaSmem = 120 * 1024;  // > half the SM's shared memory: one CTA per SM
 
-template <int N, bool FP8>
+// FORM 0: A and B K-major in shared memory (the QK^T form); FORM 1: A from Tensor Memory,
+// B MN-major in shared memory (the PV form: P from TMEM, V as stored, d contiguous)
+template <int N, bool FP8, int FORM>
 __global__ void __launch_bounds__(128, 1)
     mb_mma_kernel(int iters, unsigned long long* cycles, uint32_t* err, unsigned long long limit_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    // A: 128 rows x 128 bytes, B: N rows x 128 bytes (one swizzle atom column each, i.e.
-    // K = 64 bf16 or 128 e4m3 elements: four MMAs of K = 16 / 32), zeros
+    // FORM 0 -- A: 128 rows x 128 bytes, B: N rows x 128 bytes (one swizzle atom column
+    // each, i.e. K = 64 bf16 or 128 e4m3 elements: four MMAs of K = 16 / 32).
+    // FORM 1 -- B: 64 K rows x N columns, MN-major: N / (128 bytes) atom columns of 64 rows
+    // x 128 bytes each (8 KiB apart); A: 128 lanes x 64 K elements in TMEM columns [256, ...).
+    // All zeros.
     uint8_t* a = smem;
     uint8_t* b = smem + 128 * 128;
     uint64_t* bar = reinterpret_cast<uint64_t*>(b + N * 128);
@@ -84,9 +89,12 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_after();
     const uint32_t tmem = *tslot;
     if (threadIdx.x == 0) {
-        const uint32_t idesc = make_idesc(128, N, FP8 ? 0u : 1u, false);
+        const uint32_t idesc = make_idesc(128, N, FP8 ? 0u : 1u, FORM == 1);
         const uint64_t da = sdesc_sw128(smem_u32(a), 16, 1024);
-        const uint64_t db = sdesc_sw128(smem_u32(b), 16, 1024);
+        // MN-major B: leading offset = the next 128-byte atom column along N (8 KiB: 64 K
+        // rows of 128 bytes), stride offset = the next 8 K rows
+        const uint64_t db = FORM == 1 ? sdesc_sw128(smem_u32(b), 8192, 1024)
+                                      : sdesc_sw128(smem_u32(b), 16, 1024);
         const unsigned long long t0 = clock64();
 #pragma unroll 1
         for (int i = 0; i < iters; ++i) {
@@ -94,10 +102,19 @@ __global__ void __launch_bounds__(128, 1)
             for (int kk = 0; kk < 4; ++kk) {
                 // k step: 32 bytes (16 bf16 / 32 e4m3 elements) along the 128-byte rows
                 const uint64_t off = (uint64_t)((kk * 32) >> 4);
-                if constexpr (FP8)
+                if constexpr (FORM == 1) {
+                    // B: the next 16 (bf16) / 32 (e4m3) K rows of 128 bytes; A: the next 8
+                    // TMEM columns (32 bytes of each lane's row)
+                    const uint64_t boff = (uint64_t)((kk * (FP8 ? 32 : 16) * 128) >> 4);
+                    if constexpr (FP8)
+                        umma_f8_ts(tmem, tmem + 256u + 8u * kk, db + boff, idesc, (i | kk) != 0);
+                    else
+                        umma_f16_ts(tmem, tmem + 256u + 8u * kk, db + boff, idesc, (i | kk) != 0);
+                } else if constexpr (FP8) {
                     umma_f8_ss(tmem, da + off, db + off, idesc, (i | kk) != 0);
-                else
+                } else {
                     umma_f16_ss(tmem, da + off, db + off, idesc, (i | kk) != 0);
+                }
             }
         }
         umma_commit(smem_u32(bar));
@@ -126,19 +143,96 @@ __global__ void __launch_bounds__(128, 1)
     }
 }
 
-template <int N, bool FP8>
+template <int N, bool FP8, int FORM = 0>
 cudaError_t launch_mma(int grid, int iters, unsigned long long* cycles, uint32_t* err,
                        unsigned long long limit_ns, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(mb_mma_kernel<N, FP8>,
+    cudaError_t e = cudaFuncSetAttribute(mb_mma_kernel<N, FP8, FORM>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
     if (e != cudaSuccess) return e;
-    mb_mma_kernel<N, FP8><<<grid, 128, kMmaSmem, s>>>(iters, cycles, err, limit_ns);
+    mb_mma_kernel<N, FP8, FORM><<<grid, 128, kMmaSmem, s>>>(iters, cycles, err, limit_ns);
     return cudaGetLastError();
+}
+
+// Bulk-copy throughput into shared memory: one thread per CTA keeps kLoadSlots copies of
+// kLoadBytes in flight (cp.async.bulk, completion counted on one mbarrier per slot), each
+// from the CTA's own window of `window` bytes of `src`, read cyclically.  With a window set
+// that fits L2 (after a first pass) this is the L2 -> shared-memory rate; with a larger one,
+// the HBM read rate.
+constexpr int kLoadSlots = 4;
+constexpr int kLoadBytes = 32 * 1024;
+constexpr int kLoadSmem = kLoadSlots * kLoadBytes + 1024 + 64;
+
+__global__ void __launch_bounds__(32, 1)
+    mb_load_kernel(const uint8_t* src, unsigned long long window, int iters, unsigned long long* cycles,
+                   uint32_t* err, unsigned long long limit_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kLoadSlots * kLoadBytes);
+    if (threadIdx.x != 0) return;
+    for (int s = 0; s < kLoadSlots; ++s) mbar_init(smem_u32(bars + s), 1);
+    fence_barrier_init();
+    const uint8_t* base = src + (size_t)blockIdx.x * window;
+    const unsigned long long nchunks = window / kLoadBytes;
+    const unsigned long long t0 = clock64();
+    bool ok = true;
+    for (int i = 0; i < iters && ok; ++i) {
+        const int s = i % kLoadSlots;
+        const uint32_t bar = smem_u32(bars + s);
+        if (i >= kLoadSlots) {  // the slot's previous copy has landed
+            const uint32_t parity = (uint32_t)((i / kLoadSlots) - 1) & 1u;
+            const unsigned long long g0 = globaltimer_ns();
+            while (!mbar_try_wait(bar, parity)) {
+                if (globaltimer_ns() - g0 > limit_ns) {
+                    ok = false;
+                    break;
+                }
+            }
+        }
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar, kLoadBytes);
+        const uint8_t* g = base + (size_t)(i % nchunks) * kLoadBytes;
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                smem_u32(smem + s * kLoadBytes)),
+            "l"(g), "r"(kLoadBytes), "r"(bar)
+            : "memory");
+    }
+    // the last copies have landed (bounded), before the time is taken and the CTA retires
+    for (int i = (iters > kLoadSlots ? iters - kLoadSlots : 0); i < iters; ++i) {
+        const uint32_t bar = smem_u32(bars + (i % kLoadSlots));
+        const uint32_t parity = (uint32_t)(i / kLoadSlots) & 1u;
+        const unsigned long long g0 = globaltimer_ns();
+        while (!mbar_try_wait(bar, parity)) {
+            if (globaltimer_ns() - g0 > limit_ns) {
+                ok = false;
+                break;
+            }
+        }
+    }
+    const unsigned long long t1 = clock64();
+    if (!ok) atomicOr(err, 1u);
+    cycles[blockIdx.x] = t1 - t0;
 }
 
 }  // namespace
 
 extern "C" {
+
+int fa_mb_load(int grid, const void* src, unsigned long long window, int iters, unsigned long long* cycles,
+               uint32_t* err, unsigned long long limit_ns, void* stream) {
+    if (grid < 1 || iters < 1 || !src || !cycles || !err || window < (unsigned long long)kLoadBytes ||
+        window % kLoadBytes != 0 || (reinterpret_cast<uintptr_t>(src) & 15u) != 0)
+        return (int)cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(mb_load_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kLoadSmem);
+    if (e != cudaSuccess) return (int)e;
+    mb_load_kernel<<<grid, 32, kLoadSmem, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t*>(src), window, iters, cycles, err, limit_ns);
+    return (int)cudaGetLastError();
+}
+
+long long fa_mb_load_bytes_per_cta(int iters) { return (long long)iters * kLoadBytes; }
 
 int fa_mb_ex2(int grid, int iters, unsigned long long* cycles, float* sink, void* stream) {
     if (grid < 1 || iters < 1 || !cycles || !sink) return (int)cudaErrorInvalidValue;
@@ -157,10 +251,14 @@ int fa_mb_mma(int grid, int n, int fp8, int iters, unsigned long long* cycles, u
     if (!fp8 && n == 256) return (int)launch_mma<256, false>(grid, iters, cycles, err, limit_ns, s);
     if (fp8 && n == 128) return (int)launch_mma<128, true>(grid, iters, cycles, err, limit_ns, s);
     if (fp8 && n == 256) return (int)launch_mma<256, true>(grid, iters, cycles, err, limit_ns, s);
+    // the PV form (A from TMEM, B MN-major), N = head dim 128
+    if (!fp8 && n == -128) return (int)launch_mma<128, false, 1>(grid, iters, cycles, err, limit_ns, s);
+    if (fp8 && n == -128) return (int)launch_mma<128, true, 1>(grid, iters, cycles, err, limit_ns, s);
     return (int)cudaErrorInvalidValue;
 }
 
 long long fa_mb_mma_flops_per_cta(int n, int fp8, int iters) {
+    if (n < 0) n = -n;  // (the PV form)
     // 4 MMAs per iteration (the 128-byte rows hold K = 64 bf16 or K = 128 e4m3), each
     // 2 * M * N * K FLOPs with M = 128
     const long long k_per_mma = fp8 ? 32 : 16;

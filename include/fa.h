@@ -323,10 +323,11 @@ FA_API void fa_debug_set(uint64_t wait_limit_ns, uint32_t inject);
  * (a variant build; the default library returns FA_ERR_UNSUPPORTED and its kernel
  * holds no trace code).  buf: device memory of at least fa_debug_trace_bytes()
  * bytes, 16-byte aligned, owned by the caller (NULL stops tracing); later launches
- * make the first 8 CTAs log up to 8192 events per role into it: word
- * (cta * 4 + role) * 8192 + i = tag << 56 | clock64 (low 56 bits), roles 0 the
- * TMA producer, 1 the MMA issuer, 2 and 3 the softmax warps of query tiles 0 and
- * 1 (tags: see the kernel header).  Unwritten words keep what the caller put there.
+ * make 8 CTAs spread over the grid (slot k: CTA k * (grid - 1) / 7) log up to 8192
+ * events per role into it: word (slot * 4 + role) * 8192 + i = tag << 56 | clock64
+ * (low 56 bits), roles 0 the TMA producer, 1 the MMA issuer, 2 and 3 the softmax
+ * warps of query tiles 0 and 1 (tags: see the kernel header).  Unwritten words keep
+ * what the caller put there.
  */
 FA_API fa_status fa_debug_trace(void* buf, size_t bytes);
 FA_API size_t fa_debug_trace_bytes(void);

@@ -3,6 +3,9 @@
  * measure the two ceilings of the attention forward kernel on this GPU: the
  * MUFU exponential rate and the tcgen05 tensor-pipe rate.
  *
+ * A third probe measures how fast shared memory is fed from L2 (and HBM) by
+ * bulk copies, the path every K/V block of the forward kernel takes.
+ *
  * Why: the page "Dissecting the SM_120 Microarchitecture" (section 11.2,
  * Fig. 12) finds exp2 on the special-function unit, not the MMAs, to dominate
  * a key block of fused attention on a GPU without Tensor Memory.  A forward
@@ -45,13 +48,29 @@ FA_MB_API long long fa_mb_ex2_per_cta(int iters);
  * tcgen05.mma issue rate.  `grid` CTAs (one per SM); in each one thread
  * issues 4 x `iters` MMAs of M = 128, N = n (64, 128 or 256 for bf16; 128 or
  * 256 for e4m3) and K = 16 (bf16, kind::f16) or 32 (e4m3, kind::f8f6f4), A and
- * B from shared memory, fp32 accumulate in Tensor Memory, then waits for their
- * completion.  Writes each CTA's SM cycles to cycles[grid].
+ * B K-major from shared memory, fp32 accumulate in Tensor Memory, then waits
+ * for their completion.  n = -128: N = 128 with A read from Tensor Memory and
+ * B MN-major in shared memory (the form of the P V product).  Writes each
+ * CTA's SM cycles to cycles[grid].
  */
 FA_MB_API int fa_mb_mma(int grid, int n, int fp8, int iters, unsigned long long* cycles,
                         uint32_t* err, unsigned long long limit_ns, void* stream);
 /* FLOPs one CTA of fa_mb_mma performs (2 * M * N * K per MMA) */
 FA_MB_API long long fa_mb_mma_flops_per_cta(int n, int fp8, int iters);
+
+/*
+ * Bulk-copy (cp.async.bulk) throughput into shared memory.  `grid` CTAs; in each one
+ * thread keeps four 32 KiB copies in flight, `iters` copies in all, each from the CTA's
+ * own window of `window` bytes at src + cta * window (read cyclically; window a multiple
+ * of 32 KiB, src 16-byte aligned, grid * window bytes readable).  A window set that fits
+ * L2, read once beforehand, measures the L2 -> shared-memory rate; a larger one the HBM
+ * read rate.  Writes each CTA's SM cycles to cycles[grid].
+ */
+FA_MB_API int fa_mb_load(int grid, const void* src, unsigned long long window, int iters,
+                         unsigned long long* cycles, uint32_t* err, unsigned long long limit_ns,
+                         void* stream);
+/* bytes one CTA of fa_mb_load copies */
+FA_MB_API long long fa_mb_load_bytes_per_cta(int iters);
 
 #ifdef __cplusplus
 }

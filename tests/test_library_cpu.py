@@ -199,7 +199,8 @@ def test_microbench_library_exports_its_header():
     text = open(os.path.join(ROOT, "include", "fa_microbench.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = sorted(set(re.findall(r"\b(fa_mb_[a-z0-9_]+)\s*\(", text)))
-    assert names == ["fa_mb_ex2", "fa_mb_ex2_per_cta", "fa_mb_mma", "fa_mb_mma_flops_per_cta"]
+    assert names == ["fa_mb_ex2", "fa_mb_ex2_per_cta", "fa_mb_load", "fa_mb_load_bytes_per_cta",
+                     "fa_mb_mma", "fa_mb_mma_flops_per_cta"]
     mb = ctypes.CDLL(_build.build_microbench())
     for name in names:
         assert isinstance(getattr(mb, name), ctypes._CFuncPtr)
@@ -209,6 +210,8 @@ def test_microbench_library_exports_its_header():
     assert mb.fa_mb_mma_flops_per_cta(256, 0, 10) == 4 * 10 * 2 * 128 * 256 * 16
     assert mb.fa_mb_mma_flops_per_cta(128, 1, 10) == 4 * 10 * 2 * 128 * 128 * 32
     assert mb.fa_mb_ex2_per_cta(10) == 1024 * 8 * 4 * 10
+    mb.fa_mb_load_bytes_per_cta.restype = ctypes.c_longlong
+    assert mb.fa_mb_load_bytes_per_cta(10) == 10 * 32 * 1024
 
 
 def test_trace_is_unsupported_in_the_default_build(lib):
