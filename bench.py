@@ -160,6 +160,35 @@ def measure_load_rate(dev, window: int, iters: int = 4096) -> dict:
     return _per_sm_rates(lib.fa_mb_load_bytes_per_cta(iters), cyc.cpu().tolist())
 
 
+def measure_mma_with_load(dev, window: int = 256 << 10, iters: int = 4096) -> dict:
+    """bf16 SS-form MMA FLOP per SM clock while bulk copies stream into the same shared
+    memory, and the copies' bytes per SM clock over the same cycles."""
+    import torch
+    lib = _microbench_lib()
+    lib.fa_mb_mma_with_load.restype = ctypes.c_int
+    lib.fa_mb_mma_with_load.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_ulonglong,
+                                        ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_void_p]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    src = torch.ones(sms * window, dtype=torch.uint8, device=dev)
+    cyc = torch.zeros(sms, dtype=torch.int64, device=dev)
+    nb = torch.zeros(sms, dtype=torch.int64, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    for _ in range(2):
+        rc = lib.fa_mb_mma_with_load(sms, src.data_ptr(), window, iters, cyc.data_ptr(),
+                                     nb.data_ptr(), err.data_ptr(), 2_000_000_000, stream)
+        if rc != 0:
+            raise RuntimeError(f"fa_mb_mma_with_load launch failed ({rc})")
+    torch.cuda.synchronize(dev)
+    if int(err.item()) != 0:
+        raise RuntimeError("fa_mb_mma_with_load: a bounded wait ran out")
+    c, b = cyc.cpu().tolist(), nb.cpu().tolist()
+    flops = lib.fa_mb_mma_flops_per_cta(128, 0, iters)
+    return {"mma_flop_per_clk_per_sm": _per_sm_rates(flops, c),
+            "copy_bytes_per_clk_per_sm": statistics.median(x / y for x, y in zip(b, c) if y > 0)}
+
+
 def run_microbench(args):
     """One JSON line: ex2 and tcgen05 rates per SM clock, and what they give at the SM
     clock sampled while they ran."""
@@ -175,6 +204,7 @@ def run_microbench(args):
         mma[f"{'e4m3' if fp8 else 'bf16'}_m128_n{n}"] = measure_mma_rate(dev, n, fp8)
     for fp8 in (False, True):  # the PV form: A from Tensor Memory, B MN-major
         mma[f"{'e4m3' if fp8 else 'bf16'}_m128_n128_a_tmem_b_mn_major"] = measure_mma_rate(dev, -128, fp8)
+    mma["bf16_m128_n128_with_copies"] = measure_mma_with_load(dev)
     loads = {"l2_window_256KiB": measure_load_rate(dev, 256 << 10),
              "hbm_window_32MiB": measure_load_rate(dev, 32 << 20, iters=2048)}
     clocks = sampler.stop()
@@ -186,7 +216,7 @@ def run_microbench(args):
             "ex2_per_s_chip_at_sm_mhz": ex2["median"] * sms * mhz * 1e6,
             "mma_flop_per_clk_per_sm": mma,
             "mma_tflops_chip_at_sm_mhz": {k: v["median"] * sms * mhz * 1e6 / 1e12
-                                          for k, v in mma.items()}}
+                                          for k, v in mma.items() if "median" in v}}
     print(json.dumps(line), flush=True)
     return 0
 

@@ -215,6 +215,111 @@ __global__ void __launch_bounds__(32, 1)
     cycles[blockIdx.x] = t1 - t0;
 }
 
+// The tensor pipe and the bulk-copy engine sharing one SM's shared memory: thread 0
+// issues SS-form MMAs (M = 128, N = 128, bf16, as the QK^T product) for `iters` x 4
+// instructions while thread 32 keeps two 32 KiB bulk copies in flight from the CTA's own
+// L2-resident window (as the K/V stream) until the MMAs are done.  Reports the MMA cycles
+// and the bytes copied meanwhile.
+__global__ void __launch_bounds__(64, 1)
+    mb_mma_load_kernel(const uint8_t* src, unsigned long long window, int iters,
+                       unsigned long long* cycles, unsigned long long* bytes, uint32_t* err,
+                       unsigned long long limit_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* a = smem;                    // 16 KiB
+    uint8_t* b = smem + 16384;            // 16 KiB
+    uint8_t* ld = smem + 32768;           // 2 x 32 KiB copy slots
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 32768 + 2 * kLoadBytes);  // mma, 2 copies
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+    volatile uint32_t* done = reinterpret_cast<volatile uint32_t*>(bars + 4);
+    for (int i = threadIdx.x; i < 32768 / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 3; ++s) mbar_init(smem_u32(bars + s), 1);
+        *done = 0u;
+        fence_barrier_init();
+    }
+    fence_proxy_async_smem();
+    if (threadIdx.x < 32) {
+        tmem_alloc(smem_u32(tslot), 512);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    if (threadIdx.x == 0) {
+        const uint32_t idesc = make_idesc(128, 128, 1u, false);
+        const uint64_t da = sdesc_sw128(smem_u32(a), 16, 1024);
+        const uint64_t db = sdesc_sw128(smem_u32(b), 16, 1024);
+        const unsigned long long t0 = clock64();
+#pragma unroll 1
+        for (int i = 0; i < iters; ++i) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t off = (uint64_t)((kk * 32) >> 4);
+                umma_f16_ss(tmem, da + off, db + off, idesc, (i | kk) != 0);
+            }
+        }
+        umma_commit(smem_u32(bars));
+        const unsigned long long g0 = globaltimer_ns();
+        bool ok = true;
+        while (!mbar_try_wait(smem_u32(bars), 0u)) {
+            if (globaltimer_ns() - g0 > limit_ns) {
+                ok = false;
+                break;
+            }
+        }
+        const unsigned long long t1 = clock64();
+        if (!ok) {
+            atomicOr(err, 1u);
+            const unsigned long long g1 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(bars), 0u) && globaltimer_ns() - g1 < limit_ns) {
+            }
+        }
+        cycles[blockIdx.x] = t1 - t0;
+        *done = 1u;
+    } else if (threadIdx.x == 32) {
+        const uint8_t* base = src + (size_t)blockIdx.x * window;
+        const unsigned long long nchunks = window / kLoadBytes;
+        // copy i uses slot i & 1 and completes that slot's phase i >> 1; two in flight
+        unsigned long long issued = 0, landed = 0;
+        bool ok = true;
+        const unsigned long long g0 = globaltimer_ns();
+        while (ok) {
+            if (issued - landed == 2 || (*done && issued > landed)) {  // wait for the oldest
+                const uint32_t bar = smem_u32(bars + 1 + (landed & 1));
+                while (!mbar_try_wait(bar, (uint32_t)(landed >> 1) & 1u)) {
+                    if (globaltimer_ns() - g0 > limit_ns) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (ok) ++landed;
+                continue;
+            }
+            if (*done) break;  // (nothing in flight)
+            const int s = (int)(issued & 1);
+            const uint32_t bar = smem_u32(bars + 1 + s);
+            mbar_arrive_expect_tx(bar, kLoadBytes);
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_u32(ld + s * kLoadBytes)),
+                "l"(base + (size_t)(issued % nchunks) * kLoadBytes), "r"(kLoadBytes), "r"(bar)
+                : "memory");
+            ++issued;
+        }
+        if (!ok) atomicOr(err, 2u);
+        bytes[blockIdx.x] = landed * (unsigned long long)kLoadBytes;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -233,6 +338,21 @@ int fa_mb_load(int grid, const void* src, unsigned long long window, int iters, 
 }
 
 long long fa_mb_load_bytes_per_cta(int iters) { return (long long)iters * kLoadBytes; }
+
+int fa_mb_mma_with_load(int grid, const void* src, unsigned long long window, int iters,
+                        unsigned long long* cycles, unsigned long long* bytes, uint32_t* err,
+                        unsigned long long limit_ns, void* stream) {
+    if (grid < 1 || iters < 1 || !src || !cycles || !bytes || !err ||
+        window < (unsigned long long)kLoadBytes || window % kLoadBytes != 0 ||
+        (reinterpret_cast<uintptr_t>(src) & 15u) != 0)
+        return (int)cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(mb_mma_load_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kMmaSmem);
+    if (e != cudaSuccess) return (int)e;
+    mb_mma_load_kernel<<<grid, 64, kMmaSmem, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t*>(src), window, iters, cycles, bytes, err, limit_ns);
+    return (int)cudaGetLastError();
+}
 
 int fa_mb_ex2(int grid, int iters, unsigned long long* cycles, float* sink, void* stream) {
     if (grid < 1 || iters < 1 || !cycles || !sink) return (int)cudaErrorInvalidValue;

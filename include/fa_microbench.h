@@ -72,6 +72,17 @@ FA_MB_API int fa_mb_load(int grid, const void* src, unsigned long long window, i
 /* bytes one CTA of fa_mb_load copies */
 FA_MB_API long long fa_mb_load_bytes_per_cta(int iters);
 
+/*
+ * The tensor pipe and the bulk-copy engine sharing shared memory: in each of `grid` CTAs
+ * one thread issues 4 x `iters` bf16 MMAs (M = N = 128, K = 16, A and B K-major in
+ * shared memory: the QK^T form) while another keeps two 32 KiB bulk copies in flight from
+ * the CTA's own window (as fa_mb_load) until the MMAs complete.  Writes each CTA's MMA
+ * cycles to cycles[grid] and the bytes copied meanwhile to bytes[grid] (uint64).
+ */
+FA_MB_API int fa_mb_mma_with_load(int grid, const void* src, unsigned long long window, int iters,
+                                  unsigned long long* cycles, unsigned long long* bytes,
+                                  uint32_t* err, unsigned long long limit_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
