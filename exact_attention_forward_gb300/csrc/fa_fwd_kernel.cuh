@@ -1155,15 +1155,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(bar(C::KV_EMPTY + k_slot(j)));
                     if (j + 1 < t_hi) mbar_arrive(bar(C::KV_EMPTY + v_slot(j + 1)));
                 }
-                uint32_t sr[4][32];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) tmem_ld32(t_s + 32u * q, sr[q]);
+                uint32_t sr[128];
+                tmem_ld128(t_s, sr);
                 tmem_wait_ld();
                 float s[128];
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) s[q * 32 + i] = __uint_as_float(sr[q][i]);
+                    for (int i = 0; i < 32; ++i) s[q * 32 + i] = __uint_as_float(sr[q * 32 + i]);
                 const int col0 = j * kBN;
                 const bool masked = col0 + kBN > tile_vis_min;  // diagonal or key-tail block
                 if (masked) {
@@ -1266,9 +1265,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < kPkPerChunk; ++i) pk_all[q * kPkPerChunk + i] = pk[i];
                 }
-                tmem_st32(t_s, *reinterpret_cast<const uint32_t(*)[32]>(pk_all));
-                if constexpr (!FP8)
-                    tmem_st32(t_s + 32u, *reinterpret_cast<const uint32_t(*)[32]>(pk_all + 32));
+                if constexpr (FP8)
+                    tmem_st32(t_s, *reinterpret_cast<const uint32_t(*)[32]>(pk_all));
+                else
+                    tmem_st64(t_s, pk_all);
                 float l0, l1, l2, l3;
                 unpack_f32x2(acc0, l0, l1);
                 unpack_f32x2(acc1, l2, l3);
