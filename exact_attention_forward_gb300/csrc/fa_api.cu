@@ -621,12 +621,13 @@ fa_status fwd_impl(const FwdArgs& a) {
     const int grid = stream ? sms : (int)(n_items < sms ? n_items : sms);
     set_item_bands(p, grid);
     set_half_tail(p, grid);
+    const bool cache = a.seqused_k != nullptr;  // the kernel instance with the cache code
     if (fp8)
-        e = launch_fwd_e4m3_d128(tq, tk, tv, to, p, grid, s, append && !fused_append);
+        e = launch_fwd_e4m3_d128(tq, tk, tv, to, p, grid, s, append && !fused_append, cache);
     else if (a.head_dim == 64)
-        e = launch_fwd_bf16_d64(tq, tk, tv, to, p, grid, s, append && !fused_append);
+        e = launch_fwd_bf16_d64(tq, tk, tv, to, p, grid, s, append && !fused_append, cache);
     else
-        e = launch_fwd_bf16_d128(tq, tk, tv, to, p, grid, s, append && !fused_append);
+        e = launch_fwd_bf16_d128(tq, tk, tv, to, p, grid, s, append && !fused_append, cache);
     if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
     if (p.split) {
         e = launch_combine(p.ws_o, p.ws_lse, a.o, a.lse, a.batch, a.heads, a.seqlen_q,
