@@ -98,20 +98,25 @@ def _per_sm_rates(units_per_cta: float, cycles) -> dict:
     return {"median": statistics.median(rates), "min": rates[0], "max": rates[-1]}
 
 
-def measure_ex2_rate(dev, iters: int = 2048) -> dict:
-    """ex2.approx.ftz.f32 per SM clock (one 1024-thread CTA per SM, clock64-timed)."""
+def measure_ex2_rate(dev, iters: int = 2048, packed: bool = False) -> dict:
+    """ex2.approx.ftz.f32 per SM clock (one 1024-thread CTA per SM, clock64-timed);
+    packed: ex2.approx.f16x2, counting both halves."""
     import torch
     lib = _microbench_lib()
+    lib.fa_mb_ex2_f16x2.restype = ctypes.c_int
+    lib.fa_mb_ex2_f16x2.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                    ctypes.c_void_p]
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     cyc = torch.zeros(sms, dtype=torch.int64, device=dev)
     sink = torch.zeros(1024, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev).cuda_stream
+    fn = lib.fa_mb_ex2_f16x2 if packed else lib.fa_mb_ex2
     for _ in range(2):  # the first launch also loads the module
-        rc = lib.fa_mb_ex2(sms, iters, cyc.data_ptr(), sink.data_ptr(), stream)
+        rc = fn(sms, iters, cyc.data_ptr(), sink.data_ptr(), stream)
         if rc != 0:
-            raise RuntimeError(f"fa_mb_ex2 launch failed ({rc})")
+            raise RuntimeError(f"ex2 probe launch failed ({rc})")
     torch.cuda.synchronize(dev)
-    return _per_sm_rates(lib.fa_mb_ex2_per_cta(iters), cyc.cpu().tolist())
+    return _per_sm_rates(lib.fa_mb_ex2_per_cta(iters) * (2 if packed else 1), cyc.cpu().tolist())
 
 
 def measure_mma_rate(dev, n: int, fp8: bool, iters: int = 2048) -> dict:
@@ -199,6 +204,7 @@ def run_microbench(args):
     sampler.start()
     time.sleep(0.3)
     ex2 = measure_ex2_rate(dev)
+    ex2_f16x2 = measure_ex2_rate(dev, packed=True)
     mma = {}
     for n, fp8 in ((64, False), (128, False), (256, False), (128, True), (256, True)):
         mma[f"{'e4m3' if fp8 else 'bf16'}_m128_n{n}"] = measure_mma_rate(dev, n, fp8)
@@ -212,7 +218,7 @@ def run_microbench(args):
     line = {"microbench": "ex2 / tcgen05 / bulk-copy throughput", "sms": sms, "clocks": clocks,
             "load_bytes_per_clk_per_sm": loads,
             "load_gbs_chip_at_sm_mhz": {k: v["median"] * sms * mhz * 1e6 / 1e9 for k, v in loads.items()},
-            "ex2_per_clk_per_sm": ex2,
+            "ex2_per_clk_per_sm": ex2, "ex2_f16x2_per_clk_per_sm": ex2_f16x2,
             "ex2_per_s_chip_at_sm_mhz": ex2["median"] * sms * mhz * 1e6,
             "mma_flop_per_clk_per_sm": mma,
             "mma_tflops_chip_at_sm_mhz": {k: v["median"] * sms * mhz * 1e6 / 1e12

@@ -54,6 +54,34 @@ __global__ void __launch_bounds__(kEx2Threads, 1)
     if (s == -1.0f) sink[threadIdx.x] = s;  // never true; keeps the chains alive
 }
 
+// The same with ex2.approx.f16x2: two fp16 exponentials per instruction.
+__global__ void __launch_bounds__(kEx2Threads, 1)
+    mb_ex2_f16x2_kernel(int iters, unsigned long long* cycles, float* sink) {
+    uint32_t x[kEx2Chains];
+#pragma unroll
+    for (int u = 0; u < kEx2Chains; ++u) {
+        const float f = 0.25f + 0.01f * (float)((threadIdx.x + u) & 31);
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(x[u]) : "f"(f), "f"(f + 0.125f));
+    }
+    __syncthreads();
+    const unsigned long long t0 = clock64();
+#pragma unroll 1
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int u = 0; u < kEx2Chains; ++u)  // 2^-x for both halves: stays in (0.5, 1)
+                asm volatile("ex2.approx.f16x2 %0, %1;" : "=r"(x[u]) : "r"(x[u] ^ 0x80008000u));
+    }
+    __syncthreads();
+    const unsigned long long t1 = clock64();
+    if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
+    uint32_t s = 0;
+#pragma unroll
+    for (int u = 0; u < kEx2Chains; ++u) s ^= x[u];
+    if (s == 0xFFFFFFFFu) sink[threadIdx.x] = (float)s;  // never true; keeps the chains alive
+}
+
 constexpr int kMmaSmem = 120 * 1024;  // > half the SM's shared memory: one CTA per SM
 
 // FORM 0: A and B K-major in shared memory (the QK^T form); FORM 1: A from Tensor Memory,
@@ -357,6 +385,12 @@ int fa_mb_mma_with_load(int grid, const void* src, unsigned long long window, in
 int fa_mb_ex2(int grid, int iters, unsigned long long* cycles, float* sink, void* stream) {
     if (grid < 1 || iters < 1 || !cycles || !sink) return (int)cudaErrorInvalidValue;
     mb_ex2_kernel<<<grid, kEx2Threads, 0, static_cast<cudaStream_t>(stream)>>>(iters, cycles, sink);
+    return (int)cudaGetLastError();
+}
+
+int fa_mb_ex2_f16x2(int grid, int iters, unsigned long long* cycles, float* sink, void* stream) {
+    if (grid < 1 || iters < 1 || !cycles || !sink) return (int)cudaErrorInvalidValue;
+    mb_ex2_f16x2_kernel<<<grid, kEx2Threads, 0, static_cast<cudaStream_t>(stream)>>>(iters, cycles, sink);
     return (int)cudaGetLastError();
 }
 

@@ -43,6 +43,13 @@ FA_MB_API int fa_mb_ex2(int grid, int iters, unsigned long long* cycles, float* 
                         void* stream);
 /* exponentials one CTA of fa_mb_ex2 evaluates */
 FA_MB_API long long fa_mb_ex2_per_cta(int iters);
+/*
+ * The same for ex2.approx.f16x2 (two fp16 exponentials per instruction): the CTAs
+ * evaluate 2 x fa_mb_ex2_per_cta(iters) exponentials in as many instructions as
+ * fa_mb_ex2.
+ */
+FA_MB_API int fa_mb_ex2_f16x2(int grid, int iters, unsigned long long* cycles, float* sink,
+                              void* stream);
 
 /*
  * tcgen05.mma issue rate.  `grid` CTAs (one per SM); in each one thread

@@ -199,7 +199,7 @@ def test_microbench_library_exports_its_header():
     text = open(os.path.join(ROOT, "include", "fa_microbench.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = sorted(set(re.findall(r"\b(fa_mb_[a-z0-9_]+)\s*\(", text)))
-    assert names == ["fa_mb_ex2", "fa_mb_ex2_per_cta", "fa_mb_load", "fa_mb_load_bytes_per_cta",
+    assert names == ["fa_mb_ex2", "fa_mb_ex2_f16x2", "fa_mb_ex2_per_cta", "fa_mb_load", "fa_mb_load_bytes_per_cta",
                      "fa_mb_mma", "fa_mb_mma_flops_per_cta", "fa_mb_mma_with_load"]
     mb = ctypes.CDLL(_build.build_microbench())
     for name in names:
