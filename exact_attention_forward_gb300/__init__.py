@@ -273,12 +273,12 @@ def fwd(q, k, v, *, causal=False, softmax_scale=None, cu_seqlens_q=None, cu_seql
     if isinstance(workspace, str):
         if workspace != "auto":
             raise ValueError('workspace must be "auto", None or a uint8 CUDA tensor')
-        if not varlen:
-            need = workspace_size(batch, heads, sq_arg, sk_arg, dv, causal, heads_k=heads_k)
-            if need > 0:  # allocated from torch's caching allocator (no cudaMalloc per call)
-                ws = torch.empty(need, dtype=torch.uint8, device=dev)
-                ws_bytes = need
-                temps.append(ws)
+        # (varlen: sized by the longest sequences)
+        need = workspace_size(batch, heads, mq, mk, dv, causal, heads_k=heads_k) if mq > 0 else 0
+        if need > 0:  # allocated from torch's caching allocator (no cudaMalloc per call)
+            ws = torch.empty(need, dtype=torch.uint8, device=dev)
+            ws_bytes = need
+            temps.append(ws)
     elif workspace is not None:
         ws = workspace
         ws_bytes = workspace.numel() * workspace.element_size()

@@ -292,12 +292,18 @@ size_t workspace_bytes_for(int splits, int batch, int heads, int sq, int dv) {
 // columns of O.  The partial rows of the first batch of splits are requested together
 // with the LSEs (they do not depend on the weights), and a batch holds 12 splits, so up
 // to 12 splits take one memory round trip and up to 24 take two.
+// Packed variable-length batches (cu_q != nullptr): the partial rows are laid out by
+// (sequence, head, row < sq = the longest sequence's length); rows past a sequence's own
+// length hold nothing and are skipped, and the results go to the packed O [total_q, H, Dv]
+// and LSE [H, total_q].
 template <int DV>
 __global__ void __launch_bounds__(256) fa_combine_kernel(const float* __restrict__ ws_o,
                                                          const float* __restrict__ ws_lse,
                                                          __nv_bfloat16* __restrict__ o,
                                                          float* __restrict__ lse, int batch,
-                                                         int heads, int sq, int splits) {
+                                                         int heads, int sq, int splits,
+                                                         const int32_t* __restrict__ cu_q,
+                                                         int total_q) {
     constexpr int kCols = DV / 32;  // columns per lane
     constexpr int kBatch = 12;
     const long long rows = (long long)batch * heads * sq;
@@ -310,6 +316,14 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const float* __restrict
     const long long b = bh / heads;
     const size_t stride = (size_t)rows;  // rows per split
     const float* src = ws_o + (size_t)row * DV + lane * kCols;
+    size_t out_row = ((size_t)b * sq + i) * heads + h;     // row of O (in units of DV)
+    size_t lse_idx = ((size_t)b * heads + h) * sq + i;
+    if (cu_q) {
+        const int q0 = __ldg(cu_q + b);
+        if (i >= __ldg(cu_q + b + 1) - q0) return;  // past this sequence's rows
+        out_row = ((size_t)q0 + i) * heads + h;
+        lse_idx = (size_t)h * total_q + q0 + i;
+    }
     // launched as a programmatic dependent of the forward kernel: wait for its
     // completion (and memory) before reading the partial results
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -338,8 +352,8 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const float* __restrict
     for (int s = lane + 32; s < splits; s += 32) mx = fmaxf(mx, __ldg(ws_lse + s * stride + row));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    __nv_bfloat16* out = o + (((size_t)b * sq + i) * heads + h) * DV + lane * kCols;
-    float* lse_out = lse + ((size_t)b * heads + h) * sq + i;
+    __nv_bfloat16* out = o + out_row * DV + lane * kCols;
+    float* lse_out = lse + lse_idx;
     if (mx == -INFINITY) {  // no split saw a key: O = 0, LSE = -inf
 #pragma unroll
         for (int c = 0; c < kCols; ++c) out[c] = __float2bfloat16(0.f);
@@ -388,7 +402,8 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const float* __restrict
 }
 
 cudaError_t launch_combine(const float* ws_o, const float* ws_lse, void* o, float* lse, int batch,
-                           int heads, int seqlen_q, int dv, int n_splits, cudaStream_t s) {
+                           int heads, int seqlen_q, int dv, int n_splits, const int32_t* cu_q,
+                           int total_q, cudaStream_t s) {
     const long long rows = (long long)batch * heads * seqlen_q;
     const int threads = 256;
     const long long blocks = (rows * 32 + threads - 1) / threads;
@@ -407,9 +422,9 @@ cudaError_t launch_combine(const float* ws_o, const float* ws_lse, void* o, floa
     __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
     if (dv == 128)
         return cudaLaunchKernelEx(&cfg, fa_combine_kernel<128>, ws_o, ws_lse, ob, lse, batch, heads,
-                                  seqlen_q, n_splits);
+                                  seqlen_q, n_splits, cu_q, total_q);
     return cudaLaunchKernelEx(&cfg, fa_combine_kernel<64>, ws_o, ws_lse, ob, lse, batch, heads,
-                              seqlen_q, n_splits);
+                              seqlen_q, n_splits, cu_q, total_q);
 }
 
 // Every entry point fills one of these; fwd_impl validates and launches.
@@ -502,10 +517,13 @@ fa_status fwd_impl(const FwdArgs& a) {
     int splits = 1;
     const bool stream = a.seqused_k && a.workspace && mq > 0 &&
                         use_stream_plan(a.batch, a.heads, a.heads_k, a.seqlen_q, a.seqlen_k, a.causal, sms);
-    if (!varlen && a.workspace && mq > 0) {
-        splits = stream ? kStreamSlots
-                        : plan_splits(a.batch, a.heads, a.heads_k, a.seqlen_q, a.seqlen_k, a.causal, sms);
-        const size_t need = workspace_bytes_for(splits, a.batch, a.heads, a.seqlen_q, a.head_dim_v);
+    if (a.workspace && mq > 0 && !a.cta_pair) {
+        // (varlen: the longest lengths decide, and the partial rows are laid out by sequence
+        // with max_seqlen_q rows each; packed grouped-query tiles are not used for varlen)
+        splits = stream   ? kStreamSlots
+                 : varlen ? choose_splits(a.batch, a.heads, mq, mk, a.causal, sms)
+                          : plan_splits(a.batch, a.heads, a.heads_k, a.seqlen_q, a.seqlen_k, a.causal, sms);
+        const size_t need = workspace_bytes_for(splits, a.batch, a.heads, mq, a.head_dim_v);
         if (a.workspace_bytes < need)
             return fail(FA_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed",
                         a.workspace_bytes, need);
@@ -553,7 +571,7 @@ fa_status fwd_impl(const FwdArgs& a) {
     if (stream) p.n_items = 1;  // pieces are published as index 0, the end as index 1
     p.v_e5m2 = a.v_dtype == FA_DTYPE_E5M2 ? 1 : 0;
     if (p.split) {
-        const size_t rows = (size_t)splits * a.batch * a.heads * a.seqlen_q;
+        const size_t rows = (size_t)splits * a.batch * a.heads * mq;
         p.ws_o = static_cast<float*>(a.workspace);
         p.ws_lse = p.ws_o + rows * a.head_dim_v;
     }
@@ -630,8 +648,8 @@ fa_status fwd_impl(const FwdArgs& a) {
         e = launch_fwd_bf16_d128(tq, tk, tv, to, p, grid, s, append && !fused_append, cache);
     if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
     if (p.split) {
-        e = launch_combine(p.ws_o, p.ws_lse, a.o, a.lse, a.batch, a.heads, a.seqlen_q,
-                           a.head_dim_v, splits, s);
+        e = launch_combine(p.ws_o, p.ws_lse, a.o, a.lse, a.batch, a.heads, mq, a.head_dim_v, splits,
+                           varlen ? a.cu_q : nullptr, varlen ? a.seqlen_q : 0, s);
         if (e != cudaSuccess) return fail(FA_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
     }
     return FA_OK;
@@ -729,7 +747,15 @@ size_t fa_fwd_workspace_size_gqa(int batch, int heads, int heads_k, int seqlen_q
                                  int head_dim_v, int causal) {
     const int s = fa_fwd_num_splits_gqa(batch, heads, heads_k, seqlen_q, seqlen_k, causal);
     if (head_dim_v < 1) return 0;
-    return workspace_bytes_for(s, batch, heads, seqlen_q, head_dim_v);
+    // also enough for a packed varlen batch whose longest sequences have these lengths
+    int sv = 1, dev, sms;
+    uint32_t* err;
+    if (batch >= 1 && heads >= 1 && seqlen_q >= 1 && seqlen_k >= 1 &&
+        device_info(&dev, &sms, &err) == FA_OK)
+        sv = choose_splits(batch, heads, seqlen_q, seqlen_k, causal, sms);
+    const size_t fixed = workspace_bytes_for(s, batch, heads, seqlen_q, head_dim_v);
+    const size_t packed = workspace_bytes_for(sv, batch, heads, seqlen_q, head_dim_v);
+    return fixed > packed ? fixed : packed;
 }
 
 int fa_fwd_kvcache_num_splits(int batch, int heads, int heads_k, int seqlen_q, int cache_capacity,

@@ -97,9 +97,10 @@ cudaError_t max_resident_pairs_bf16_d128(int* pairs);
 cudaError_t launch_append_kv(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                              const int32_t* cache_seqlens, int batch, int capacity, int n_new,
                              long long row_bytes, uint32_t* err, cudaStream_t s);
+// (cu_q: packed varlen offsets on the device, or nullptr; total_q: packed query rows)
 cudaError_t launch_combine(const float* ws_o, const float* ws_lse, void* o, float* lse,
                            int batch, int heads, int seqlen_q, int dv, int n_splits,
-                           cudaStream_t s);
+                           const int32_t* cu_q, int total_q, cudaStream_t s);
 // Records `msg` as this thread's fa_last_error_detail() and returns `status` (for entry
 // points outside fa_api.cu).
 fa_status set_error_detail(fa_status status, const char* msg);

@@ -89,8 +89,11 @@ typedef enum {
  *   v_descale.  Descale pointers must be NULL for FA_DTYPE_BF16.
  * workspace: optional device scratch for splitting long key ranges over
  *   several CTAs (short-query / long-key shapes).  NULL disables splitting.
- *   If non-NULL it must hold fa_fwd_workspace_size(...) bytes, else
- *   FA_ERR_WORKSPACE.  Fixed-length inputs only; ignored for varlen.
+ *   If non-NULL it must hold fa_fwd_workspace_size(batch, heads,
+ *   max_seqlen_q, max_seqlen_k, head_dim_v, causal) bytes, else
+ *   FA_ERR_WORKSPACE.  For varlen the longest lengths decide whether and how
+ *   far the key range is split, and the partial results are laid out per
+ *   sequence with max_seqlen_q rows each.
  * stream: cudaStream_t.
  */
 FA_API fa_status fa_fwd(const void* q, const void* k, const void* v,
@@ -224,10 +227,13 @@ FA_API fa_status fa_fwd_kvcache(const void* q, void* k_cache, void* v_cache,
                                 void* stream);
 
 /*
- * Bytes of workspace that fa_fwd would use to split the key range of a
- * fixed-length problem of this shape on the current device (0 = it would not
- * split).  Splitting follows the log-sum-exp merge identity: each split
- * writes a normalised partial O and its LSE, a second kernel merges them.
+ * Bytes of workspace that fa_fwd would use to split the key range of a problem
+ * of this shape on the current device (0 = it would not split): a fixed-length
+ * problem, or a packed varlen batch whose longest sequences have lengths
+ * seqlen_q / seqlen_k (max_seqlen_q / max_seqlen_k).  Splitting follows the
+ * log-sum-exp merge identity: each split writes a normalised partial O and its
+ * LSE, a second kernel merges them.  `causal` is accepted for the split rule;
+ * the current rule does not depend on it.
  */
 FA_API size_t fa_fwd_workspace_size(int batch, int heads, int seqlen_q, int seqlen_k,
                              int head_dim_v, int causal);

@@ -131,6 +131,24 @@ def test_shortq_longkv_split_and_unsplit():
     compare(o_n, lse_n, o_ref, lse_ref, what="short-q long-kv, unsplit")
 
 
+@pytest.mark.parametrize("D,causal", [(128, False), (128, True), (64, False)])
+def test_varlen_split(D, causal):
+    # a packed batch of short query blocks against long (and empty) key ranges: the key
+    # range is split over CTAs as for fixed-length shapes, with the partial rows laid out
+    # per sequence (max_seqlen_q rows each) and merged into the packed outputs
+    sq = [1, 37, 0, 128, 5]
+    sk = [20000, 5000, 3000, 30000, 0]
+    x = inputs.make_varlen(sq, sk, heads=4, head_dim=D, seed=61 + D)
+    assert fa.num_splits(len(sq), 4, max(sq), max(sk), causal) > 1
+    o_s, lse_s = run_gpu(x, causal=causal, softmax_scale=D ** -0.5, workspace="auto")
+    o_n, lse_n = run_gpu(x, causal=causal, softmax_scale=D ** -0.5, workspace=None)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=D ** -0.5,
+                                      causal=causal, cu_seqlens_q=x["cu_seqlens_q"],
+                                      cu_seqlens_k=x["cu_seqlens_k"])
+    compare(o_s, lse_s, o_ref, lse_ref, what=f"varlen split D={D} causal={causal}")
+    compare(o_n, lse_n, o_ref, lse_ref, what=f"varlen unsplit D={D} causal={causal}")
+
+
 def test_split_causal_small():
     # causal with a short query block against a long key range: splits whose
     # key range lies beyond every row's diagonal produce -inf partials
