@@ -529,10 +529,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool withheld = false;
             bool aborted = false;
             uint32_t published = 0;
-            // decodes item w (an index below p.n_items) into `it` and publishes both
-            auto publish = [&](int w, Item& it) -> bool {
+            // a pair's two producers follow one static order (no device counter)
+            const bool greedy = !PAIR && p.greedy;
+            // decodes item w (an index below p.n_items) into `it` and publishes both; in the
+            // greedy hand-out an item with no rows (a tile pair past a short sequence's end) is
+            // passed over for the next ticket instead of going round the item ring (varlen
+            // -3 %; not in the FP8 instance, whose code measured 2.3 % slower with it)
+            auto publish = [&](int& w, Item& it) -> bool {
                 const uint32_t slot = published & 1u;
-                if (!(CACHE && p.stream) && w < p.n_items) it = decode_item<PAIR, CACHE>(p, w, rank);
+                if (!(CACHE && p.stream)) {
+                    while (w < p.n_items) {
+                        it = decode_item<PAIR, CACHE>(p, w, rank);
+                        if (FP8 || !greedy || it.active[0] || it.active[1]) break;
+                        w = min((int)(gridDim.x + atomicAdd(p.sched, 1u)), p.n_items);
+                    }
+                }
                 if (published >= 2 &&
                     !wait_bar(bar(C::ITEM_EMPTY + slot), ((published >> 1) - 1) & 1u, wc, SITE_ITEM_EMPTY))
                     return false;
@@ -553,8 +564,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p.sched[1] = 0u;
                 }
             };
-            // a pair's two producers follow one static order (no device counter)
-            const bool greedy = !PAIR && p.greedy;
             // Balanced cache plan (p.stream): the key blocks of all items, concatenated in
             // (batch, item head) order, are cut into equal shares of T blocks, one per CTA:
             // this CTA runs the pieces of the items that overlap [lo_g, hi_g), each in its own

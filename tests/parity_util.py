@@ -211,3 +211,31 @@ def gather_rows(o, lse, rows, varlen=False, cu_q=None):
         pos = np.asarray(cu_q, dtype=np.int64)[b] + i
         return o[pos, h], lse[h, pos]
     return o[b, i, h], lse[b, h, i]
+
+
+def e4m3_half_spacing(p: np.ndarray) -> np.ndarray:
+    """Half the spacing of e4m3 values around p >= 0 (round to nearest): 3 mantissa bits in
+    the normal range [2^-6, 448], spacing 2^-9 below it (subnormals, and values that round
+    to zero)."""
+    p = np.asarray(p, dtype=np.float64)
+    out = np.full(p.shape, 2.0 ** -10)
+    nrm = p >= 2.0 ** -6
+    out[nrm] = np.exp2(np.floor(np.log2(p[nrm])) - 4.0)
+    return out
+
+
+def fp8_p_bound(w: np.ndarray, v_abs: np.ndarray, lags=np.linspace(0.0, 8.0, 33)) -> np.ndarray:
+    """Worst-case change of O from rounding P to e4m3, for rows with softmax weights w [n, Sk]
+    over keys with |V| v_abs [Sk, Dv] (or [n, Sk, Dv]): the kernel exponentiates against a
+    reference maximum that lags the row's maximum by up to 2^8, so P_j = 2^lag w_j / w_max and
+    the normaliser is L = 2^lag / w_max; each P_j moves by at most half an e4m3 spacing, and
+    |dO_d| <= sum_j hs(P_j) |v_jd| / L.  Returns the largest bound over the lags, [n, Dv]."""
+    w = np.asarray(w, dtype=np.float64)
+    wmax = np.maximum(w.max(axis=1, keepdims=True), 1e-300)
+    best = None
+    for lag in lags:
+        p = np.exp2(lag) * w / wmax
+        hs = np.where(w > 0, e4m3_half_spacing(p), 0.0) * wmax / np.exp2(lag)
+        b = np.einsum("nk,nkd->nd", hs, v_abs) if v_abs.ndim == 3 else hs @ v_abs
+        best = b if best is None else np.maximum(best, b)
+    return best

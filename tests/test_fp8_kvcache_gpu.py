@@ -14,7 +14,8 @@ import torch
 import oracle
 import exact_attention_forward_gb300 as fa
 from exact_attention_forward_gb300 import inputs
-from parity_util import compare, nan_outputs, oracle_full, run_gpu, workload_inputs
+from parity_util import (RECORDS, compare, fp8_p_bound, half_ulp_bf16, nan_outputs,
+                         oracle_full, run_gpu, workload_inputs)
 
 pytestmark = pytest.mark.gpu
 
@@ -28,13 +29,13 @@ def _built():
 
 
 # ---------------------------------------------------------------------------- FP8
-def _fp8_head_inputs(B, H, Hk, Sq, Sk, v_dtype, seed):
-    """N(0,1) rows scaled per (batch, head) by factors in [0.75, 1] (so that every
-    (batch, K/V head) gets a different descale while the values keep the spread of
-    the FP8 workload, for which the 6e-2 bound is stated), quantised per (batch,
-    K/V head)."""
+def _fp8_head_inputs(B, H, Hk, Sq, Sk, v_dtype, seed, lo=0.75, hi=1.0):
+    """N(0,1) rows scaled per (batch, head) by factors in [lo, hi] (by default [0.75, 1],
+    so that every (batch, K/V head) gets a different descale while the values keep the
+    spread of the FP8 workload, for which the 6e-2 bound is stated), quantised per
+    (batch, K/V head)."""
     g = torch.Generator().manual_seed(seed)
-    f = lambda heads: 0.75 + 0.25 * torch.rand((B, 1, heads, 1), generator=g)
+    f = lambda heads: lo + (hi - lo) * torch.rand((B, 1, heads, 1), generator=g)
     q = torch.randn((B, Sq, H, 128), generator=g) * f(H)
     k = torch.randn((B, Sk, Hk, 128), generator=g) * f(Hk)
     v = torch.randn((B, Sk, Hk, 128), generator=g) * f(Hk)
@@ -66,6 +67,38 @@ def test_fp8_head_descales_full(B, H, Hk, Sq, Sk, causal, v_dtype):
     o1, lse1 = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=128 ** -0.5, causal=causal,
                                 descale=tuple(float(d[0, 0]) for d in x["descale"]))
     assert np.abs(lse1 - lse_ref).max() > 0.1
+
+
+def test_fp8_wide_spread_within_the_derived_bound():
+    # Values up to 1.5 N(0,1) per head: the e4m3 rounding of P (relative 2^-4, more below
+    # e4m3's normal range) then moves O past the 6e-2 stated for the N(0,1) workload.  Each
+    # element is held instead to the worst-case bound of that rounding (fp8_p_bound: half an
+    # e4m3 spacing per P_j, for any lag of the kernel's reference maximum up to 2^8, over
+    # the dequantised |V|), computed from the oracle's softmax weights, plus half a bf16 ulp
+    # of the output and 1e-3 for the fp32 arithmetic.
+    B, H, Hk, Sq, Sk, D = 2, 4, 2, 200, 400, 128
+    x = _fp8_head_inputs(B, H, Hk, Sq, Sk, "e5m2", seed=230, lo=1.0, hi=1.5)
+    o, lse = run_gpu(x, causal=False, softmax_scale=D ** -0.5)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=D ** -0.5,
+                                      descale=x["descale"])
+    assert np.abs(lse - lse_ref).max() <= 1e-3
+    rows = oracle.all_rows(B, H, seqlen_q=Sq)
+    _, _, w = oracle.attention_rows(x["q"], x["k"], x["v"], rows, softmax_scale=D ** -0.5,
+                                    descale=x["descale"], return_probs=True)
+    v8 = x["v"].view(torch.uint8).numpy()
+    v_deq = oracle.decode(v8, oracle.DT_E5M2) * x["descale"][2].numpy()[:, None, :, None]
+    bound = np.zeros_like(o)
+    g = H // Hk
+    for b in range(B):
+        for h in range(H):
+            sel = (rows[:, 0] == b) & (rows[:, 1] == h)
+            bound[b, rows[sel, 2], h] = fp8_p_bound(w[sel, :Sk], np.abs(v_deq[b, :, h // g]))
+    bound += half_ulp_bf16(o_ref) + 1e-3
+    err = np.abs(o - o_ref)
+    assert np.all(err <= bound), float((err - bound).max())
+    RECORDS.append(("fp8 1.0-1.5 N(0,1) per head, E5M2 V", "e4m3", float(err.max()),
+                    float(np.abs(lse - lse_ref).max()), float(np.abs(o_ref).max()),
+                    "derived e4m3-P bound (median %.3f)" % float(np.median(bound)), int(rows.shape[0])))
 
 
 def test_fp8_headscale_workload_full():
