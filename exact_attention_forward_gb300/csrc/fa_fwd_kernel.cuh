@@ -130,9 +130,11 @@ constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: x + magic rounds x to
 // p.trace[(slot * kTraceRoles + role) * kTraceCap + i], up to kTraceCap events each.  Tags:
 //   producer: 1 item start, 2 + t Q_EMPTY[t] passed, 4 K/V group issued, 5 next item published
 //   issuer:   1 item read, 2 Q ready, 3 K/V group ready, 4 + t P[t] ready, 6 + t tile t's
-//             MMAs of a block issued, 8 item done
+//             MMAs of a block issued, 8 item done; just before the K/V-group and P waits,
+//             11 / 12 the group had / had not landed, 13 / 14 P was / was not handed over
 //   softmax:  1 item read, 2 S ready, 3 P handed over, 4 O ready, 5 O released (TMEM),
-//             6 epilogue done
+//             6 epilogue done; within a block, 7 S in registers, 8 max and rescale done,
+//             9 exponentials done, 10 P stored to TMEM
 //   every role, first and last: 15 %globaltimer (ns), then 14 clock64 -- ties the SM's
 //   cycle count to wall time across SMs
 struct Tracer {
@@ -969,6 +971,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 for (int j = j0; j >= lo; --j) {
                     const uint32_t vslot = ring % C::kStages;
+#ifdef FA_TRACE  // had the group landed when the issuer got here?
+                    tr.ev(mbar_test_wait(bar(C::KV_FULL + vslot), (ph_kv >> vslot) & 1u) ? 11 : 12);
+#endif
                     if (!wait_kv(vslot)) {  // group {V(j), K(j-1)} (or {V(lo)})
                         aborted = true;
                         break;
@@ -988,6 +993,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const bool cur = j < hi;
                         const bool nxt = has_next && (j - 1) < hi;
                         if (cur) {
+#ifdef FA_TRACE  // was P ready when the issuer got here?
+                            tr.ev(mbar_test_wait(bar(C::P_FULL + t), (ph_p >> t) & 1u) ? 13 : 14);
+#endif
                             if (!wait_handoff(bar(C::P_FULL + t), (ph_p >> t) & 1u, SITE_P_FULL)) return false;
                             tr.ev(4 + t);
                             ph_p ^= 1u << t;
@@ -1172,6 +1180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t sr[128];
                 tmem_ld128(t_s, sr);
                 tmem_wait_ld();
+                tr.ev(7);
                 float s[128];
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
@@ -1227,6 +1236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const float mu = (m_run == -INFINITY) ? 0.0f : m_run;
+                tr.ev(8);
                 // exp2(s * scale_log2 - mu) on packed fp32 pairs (f32x2 FMA/add halve the
                 // issue slots); P is converted to bf16x2 / e4m3x4 and stored to TMEM in one go.
                 const uint64_t sc2 = f32x2(scale_log2, scale_log2);
@@ -1279,6 +1289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < kPkPerChunk; ++i) pk_all[q * kPkPerChunk + i] = pk[i];
                 }
+                tr.ev(9);
                 if constexpr (FP8)
                     tmem_st32(t_s, *reinterpret_cast<const uint32_t(*)[32]>(pk_all));
                 else
@@ -1288,6 +1299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 unpack_f32x2(acc1, l2, l3);
                 l_run += (l0 + l1) + (l2 + l3);
                 tmem_wait_st();
+                tr.ev(10);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
