@@ -640,12 +640,14 @@ fa_status fwd_impl(const FwdArgs& a) {
     set_item_bands(p, grid);
     set_half_tail(p, grid);
     const bool cache = a.seqused_k != nullptr;  // the kernel instance with the cache code
+    // the instance with packed variable-length batches (and debug injection)
+    const bool var = p.varlen || p.inject != 0u;
     if (fp8)
-        e = launch_fwd_e4m3_d128(tq, tk, tv, to, p, grid, s, append && !fused_append, cache);
+        e = launch_fwd_e4m3_d128(tq, tk, tv, to, p, grid, s, append && !fused_append, cache, var);
     else if (a.head_dim == 64)
-        e = launch_fwd_bf16_d64(tq, tk, tv, to, p, grid, s, append && !fused_append, cache);
+        e = launch_fwd_bf16_d64(tq, tk, tv, to, p, grid, s, append && !fused_append, cache, var);
     else
-        e = launch_fwd_bf16_d128(tq, tk, tv, to, p, grid, s, append && !fused_append, cache);
+        e = launch_fwd_bf16_d128(tq, tk, tv, to, p, grid, s, append && !fused_append, cache, var);
     if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
     if (p.split) {
         e = launch_combine(p.ws_o, p.ws_lse, a.o, a.lse, a.batch, a.heads, mq, a.head_dim_v, splits,

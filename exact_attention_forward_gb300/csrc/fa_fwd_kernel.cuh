@@ -234,6 +234,16 @@ struct Item {
     int fill;            // balanced plan: partial slots after this piece's to mark empty
 };
 
+// Features that only the variable-length kernel instances carry (VAR = true): packed
+// variable-length batches with their greedy hand-out, and debug injection.  With
+// VAR = false the accessors return the defaults (fixed length, no injection) as
+// compile-time constants, and the code behind them drops out.
+template <bool VAR>
+struct Var {
+    static __device__ __forceinline__ bool varlen(const FwdParams& p) { return VAR && p.varlen; }
+    static __device__ __forceinline__ uint32_t inject(const FwdParams& p) { return VAR ? p.inject : 0u; }
+};
+
 // Tile rows and visited key blocks [n_lo, n_hi_t[t]) of an item whose rows start at
 // (packed) row mp * kTiles * kSlotRows and whose key range is [n_lo, n_end), under the
 // causal mask when set (bottom-right aligned).
@@ -270,8 +280,9 @@ __device__ __forceinline__ void set_tile_ranges(const FwdParams& p, Item& it, in
 // last levels, the small items, in plain LPT order.  Query heads sharing a K/V head
 // (grouped-query attention) are consecutive items, so they stream the same K/V at
 // about the same time and share it in L2.
-template <bool PAIR, bool CACHE>
+template <bool PAIR, bool CACHE, bool VAR>
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int w, uint32_t rank) {
+    using V = Var<VAR>;
     Item it;
     it.fill = 0;
     int half = -1;  // a single query tile (0 or 1) of a tile pair item, or -1: the pair
@@ -303,7 +314,7 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int w, uint32_t 
     const int bh = r / p.n_splits;
     it.h = (bh % p.item_heads) * G;
     it.b = bh / p.item_heads;
-    if (p.varlen) {
+    if (V::varlen(p)) {
         it.q_row0 = __ldg(p.cu_q + it.b);
         it.sq = __ldg(p.cu_q + it.b + 1) - it.q_row0;
         it.k_row0 = __ldg(p.cu_k + it.b);
@@ -419,14 +430,21 @@ enum : uint32_t {
 };
 
 // CACHE: the instance for key/value-cache calls (per-sequence cache lengths, new rows
-// written by the producers, the balanced plan); the other instance holds none of that code
+// written by the producers, the balanced plan); the other instances hold none of that code
 // -- measured, the smaller kernel starts its launches faster (causal 2K -8 %).
-template <int D, bool FP8, bool PAIR = false, bool CACHE = false>
+// VAR: the instance for packed variable-length batches (and debug injection); the
+// fixed-length instance (VAR = false) leaves their code out -- measured, same-run A/B with
+// bit-identical outputs: causal 2K -1 %, FP8 4K -1.3 %, short-q/long-k -1.5 %, a
+// launch-bound B=1 H=2 S=256 call -15 to -24 %, the 8K shapes within +-0.6 %.  (Folding key
+// splits and packed rows as well made the code smaller still but the 8K launches 1.4-4 %
+// slower.)
+template <int D, bool FP8, bool PAIR = false, bool CACHE = false, bool VAR = true>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdParams p) {
     using C = Cfg<D, FP8, PAIR>;
+    using V = Var<VAR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -532,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool aborted = false;
             uint32_t published = 0;
             // a pair's two producers follow one static order (no device counter)
-            const bool greedy = !PAIR && p.greedy;
+            const bool greedy = !PAIR && VAR && p.greedy;
             // decodes item w (an index below p.n_items) into `it` and publishes both; in the
             // greedy hand-out an item with no rows (a tile pair past a short sequence's end) is
             // passed over for the next ticket instead of going round the item ring (varlen
@@ -541,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t slot = published & 1u;
                 if (!(CACHE && p.stream)) {
                     while (w < p.n_items) {
-                        it = decode_item<PAIR, CACHE>(p, w, rank);
+                        it = decode_item<PAIR, CACHE, VAR>(p, w, rank);
                         if (FP8 || !greedy || it.active[0] || it.active[1]) break;
                         w = min((int)(gridDim.x + atomicAdd(p.sched, 1u)), p.n_items);
                     }
@@ -662,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tr.ev(1);
                 const uint32_t ticket = greedy ? atomicAdd(p.sched, 1u) : 0u;
                 const Item it = it_next;
-                const int bc = p.varlen ? 0 : it.b;  // batch coordinate of the 4-D view
+                const int bc = V::varlen(p) ? 0 : it.b;  // batch coordinate of the 4-D view
                 auto load_q = [&](auto tc) -> bool {
                     constexpr int t = decltype(tc)::value;
                     if (it.n_hi_t[t] <= it.n_lo) return true;
@@ -670,12 +688,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         return false;
                     tr.ev(2 + t);
                     ph_qe ^= 1u << t;
-                    if (p.inject == 1u && !withheld) {  // debug: never arrive on this Q tile
+                    if (V::inject(p) == 1u && !withheld) {  // debug: never arrive on this Q tile
                         withheld = true;
                         return true;
                     }
                     // packed mode: the map's box spans G heads x 128/G rows
-                    const int qrow = (p.varlen ? it.q_row0 : 0) + it.m0[t] / p.pack;
+                    const int qrow = (V::varlen(p) ? it.q_row0 : 0) + it.m0[t] / p.pack;
                     // a pair's Q tiles both land on the even CTA's barrier, which expects them
                     if (rank == 0u) {
                         mbar_arrive_expect_tx(bar(C::Q_FULL + t), (PAIR ? 2 : 1) * C::kTileBytes);
@@ -712,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 };
                 auto load_kv = [&](uint32_t pos, bool is_v, int j, uint32_t full) {
                     const uint32_t dst = s_kv + (pos % C::kStages) * C::kSlotBytes;
-                    const int row = (p.varlen ? it.k_row0 : 0) + j * kBN;
+                    const int row = (V::varlen(p) ? it.k_row0 : 0) + j * kBN;
                     if constexpr (PAIR) {
                         // this CTA's half: head-dim columns [64r, 64r+64) of V(j) (one atom
                         // column, 128 keys), or keys [64r, 64r+64) of K(j) (64-row boxes)
@@ -1075,7 +1093,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const size_t rid = (((size_t)split * p.batch + b) * p.heads + hrow) * (size_t)p.seqlen_q + row;
                 lse_ptr = p.ws_lse + rid;
                 wso_ptr = p.ws_o + rid * D;
-            } else if (p.varlen) {
+            } else if (V::varlen(p)) {
                 lse_ptr = p.lse + (size_t)hrow * p.total_q + q_row0 + row;
                 o_ptr = reinterpret_cast<__nv_bfloat16*>(p.o) + (((size_t)q_row0 + row) * p.heads + hrow) * D;
             } else {
@@ -1342,7 +1360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the fp32 split partials use plain stores instead.
             // (in a pair, the odd CTA's tile of the last slot may lie wholly past the end)
             const int sq_rows = io.sq << p.pack_shift;
-            const bool use_tma = !p.split && o_m0 < sq_rows && (!p.varlen || o_m0 + kBM <= sq_rows);
+            const bool use_tma = !p.split && o_m0 < sq_rows && (!V::varlen(p) || o_m0 + kBM <= sq_rows);
             if (use_tma) {
                 // O leaves TMEM first (normalised and packed to bf16 on the way), so the MMA
                 // issuer gets it back (O_EMPTY) before any staging
@@ -1400,8 +1418,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(bar(C::STG_FULL + t));
                     if (r_in_tile == 0) {
                         if (wait_bar(bar(C::STG_FULL + t), stg_cnt & 1u, wc, SITE_STG_FULL)) {
-                            tma_store_4d(&tm_o, stile, hh * 64, io.h, (p.varlen ? io.q_row0 : 0) +
-                                         (o_m0 >> p.pack_shift), p.varlen ? 0 : io.b);
+                            tma_store_4d(&tm_o, stile, hh * 64, io.h, (V::varlen(p) ? io.q_row0 : 0) +
+                                         (o_m0 >> p.pack_shift), V::varlen(p) ? 0 : io.b);
                             bulk_commit_group();
                             if (hh + 1 < D / 64) {
                                 bulk_wait_group_read0();
@@ -1491,7 +1509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool FP8, bool PAIR = false, bool CACHE = false>
+template <int D, bool FP8, bool PAIR = false, bool CACHE = false, bool VAR = true>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t stream,
                        bool after_append) {
@@ -1505,13 +1523,13 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
     if (e != cudaSuccess) return e;
     const unsigned long long ctx = current_context_id();
     if (dev < 0 || dev >= 64 || ctx == 0 || attr_ctx[dev].load(std::memory_order_acquire) != ctx) {
-        e = cudaFuncSetAttribute(fa_fwd_kernel<D, FP8, PAIR, CACHE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(fa_fwd_kernel<D, FP8, PAIR, CACHE, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_ctx[dev].store(ctx, std::memory_order_release);
     }
     if (!after_append && !PAIR) {
-        fa_fwd_kernel<D, FP8, PAIR, CACHE><<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, o, p);
+        fa_fwd_kernel<D, FP8, PAIR, CACHE, VAR><<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, o, p);
         return cudaGetLastError();
     }
     // after the cache append: programmatic dependent launch, so this grid's set-up
@@ -1539,7 +1557,7 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, FP8, PAIR, CACHE>, q, k, v, o, p);
+    return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, FP8, PAIR, CACHE, VAR>, q, k, v, o, p);
 }
 
 // How many CTA pairs of the kernel can be resident at once (0 if none).

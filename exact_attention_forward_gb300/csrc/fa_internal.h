@@ -78,16 +78,18 @@ constexpr size_t kTraceBytes = (size_t)kTraceCtas * kTraceRoles * kTraceCap * si
 // Kernel instances (one translation unit each).
 // q, k, v: TMA load maps; o: TMA store map of the bf16 output (same 4-D view as q);
 // after_append: launched right behind the cache-append kernel on the same stream;
-// cache: a key/value-cache call (p.seqused_k set): the instance that holds the cache code
+// cache: a key/value-cache call (p.seqused_k set): the instance that holds the cache code;
+// var: otherwise, a call with packed variable-length batches or debug injection (false: the
+// fixed-length instance, which leaves that code out)
 cudaError_t launch_fwd_bf16_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                 const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t s,
-                                bool after_append, bool cache);
+                                bool after_append, bool cache, bool var);
 cudaError_t launch_fwd_bf16_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                  const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t s,
-                                bool after_append, bool cache);
+                                bool after_append, bool cache, bool var);
 cudaError_t launch_fwd_e4m3_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                  const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t s,
-                                bool after_append, bool cache);
+                                bool after_append, bool cache, bool var);
 // CTA-pair variant (bf16, D = 128; no packing, splits or cache lengths): grid = 2 x pairs,
 // launched as clusters of two; k is a map with 64-row boxes (half a key block)
 cudaError_t launch_fwd_pair_bf16_d128(const CUtensorMap& q, const CUtensorMap& k,
