@@ -30,7 +30,7 @@ import threading
 
 __all__ = ["fwd", "fwd_kvcache", "fa_fwd", "FaError", "workspace_size", "num_splits",
            "kvcache_workspace_size", "kvcache_num_splits",
-           "device_error", "debug_set", "library_path", "EXPORTED_SYMBOLS", "load_library"]
+           "device_error", "debug_set", "debug_select_steady", "library_path", "EXPORTED_SYMBOLS", "load_library"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_fa_gb300.so")
@@ -45,7 +45,7 @@ EXPORTED_SYMBOLS = ("fa_fwd", "fa_fwd_workspace_size", "fa_fwd_num_splits", "fa_
                     "fa_fwd_static_workspace", "fa_fwd_gqa", "fa_fwd_fp8", "fa_fwd_kvcache",
                     "fa_fwd_workspace_size_gqa", "fa_fwd_num_splits_gqa", "fa_fwd_2cta",
                     "fa_fwd_kvcache_workspace_size", "fa_fwd_kvcache_num_splits",
-                    "fa_debug_trace", "fa_debug_trace_bytes")
+                    "fa_debug_trace", "fa_debug_trace_bytes", "fa_debug_select_steady")
 
 _lock = threading.Lock()
 _lib = None
@@ -93,6 +93,8 @@ def load_library():
         lib.fa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         lib.fa_debug_set.restype = None
         lib.fa_debug_set.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
+        lib.fa_debug_select_steady.restype = None
+        lib.fa_debug_select_steady.argtypes = [i32]
         lib.fa_debug_trace.restype = i32
         lib.fa_debug_trace.argtypes = [vp, sz]
         lib.fa_debug_trace_bytes.restype = sz
@@ -165,6 +167,12 @@ def device_error(clear: bool = True):
 
 def debug_set(wait_limit_ns: int = 0, inject: int = 0) -> None:
     load_library().fa_debug_set(int(wait_limit_ns), int(inject))
+
+
+def debug_select_steady(mode: int = 0) -> None:
+    """Kernel instance of fixed-length bf16 head_dim-128 launches: 0 by size (default),
+    1 always the steady-block instance, -1 never (fa_debug_select_steady)."""
+    load_library().fa_debug_select_steady(int(mode))
 
 
 def _ptr(t):

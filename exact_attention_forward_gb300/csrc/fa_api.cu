@@ -38,6 +38,7 @@ thread_local char t_detail[512] = "";
 std::mutex g_mu;
 uint64_t g_wait_limit_ns = kDefaultWaitNs;
 uint32_t g_inject = 0;
+int g_steady_mode = 0;  // fa_debug_select_steady
 uint64_t* g_trace = nullptr;  // event log of a FA_TRACE build (fa_debug_trace)
 int g_num_sms[kMaxDevices] = {0};
 // Device addresses of the library's __device__ variables, valid for the context they were
@@ -50,6 +51,9 @@ uint32_t* g_sched_addr[kMaxDevices] = {nullptr};
 // a CUDA graph keep their slot for every replay, so they take theirs from the separate
 // range [kEagerSlots, kSchedSlots) and never share one with an eager launch.
 constexpr int kEagerSlots = 192;
+// (tile, key block) steps per CTA from which a fixed-length bf16 D = 128 launch takes the
+// kernel instance specialised for steady key blocks
+constexpr double kSteadyMinTileBlocksPerCta = 256.0;
 std::atomic<uint32_t> g_sched_next{0};
 std::atomic<uint32_t> g_sched_next_captured{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -575,11 +579,13 @@ fa_status fwd_impl(const FwdArgs& a) {
         p.ws_o = static_cast<float*>(a.workspace);
         p.ws_lse = p.ws_o + rows * a.head_dim_v;
     }
+    int steady_mode = 0;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         p.wait_limit_ns = g_wait_limit_ns;
         p.inject = g_inject;
         p.trace = g_trace;
+        steady_mode = g_steady_mode;
     }
 
     // ---------------------------------------------------------------- tensor maps
@@ -642,12 +648,20 @@ fa_status fwd_impl(const FwdArgs& a) {
     const bool cache = a.seqused_k != nullptr;  // the kernel instance with the cache code
     // the instance with packed variable-length batches (and debug injection)
     const bool var = p.varlen || p.inject != 0u;
+    // Long fixed-length bf16 D = 128 launches take the instance whose issuer runs the middle
+    // key blocks of an item without per-block tests.  Its extra code is fetched from DRAM on
+    // every launch after an L2 flush, so it pays off only over enough (tile, key block)
+    // steps per CTA: measured faster at causal 8K (~860 per CTA), slower at causal 2K (~54).
+    const double tile_blocks = (double)a.batch * p.item_heads * (double)ceil_div((long long)mq * pack, 128) *
+                               (double)nblk * (a.causal ? 0.5 : 1.0);
+    const bool steady = !fp8 && a.head_dim == 128 && !var && !cache && steady_mode >= 0 &&
+                        (steady_mode == 1 || tile_blocks >= kSteadyMinTileBlocksPerCta * (double)grid);
     if (fp8)
         e = launch_fwd_e4m3_d128(tq, tk, tv, to, p, grid, s, append && !fused_append, cache, var);
     else if (a.head_dim == 64)
         e = launch_fwd_bf16_d64(tq, tk, tv, to, p, grid, s, append && !fused_append, cache, var);
     else
-        e = launch_fwd_bf16_d128(tq, tk, tv, to, p, grid, s, append && !fused_append, cache, var);
+        e = launch_fwd_bf16_d128(tq, tk, tv, to, p, grid, s, append && !fused_append, cache, var, steady);
     if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
     if (p.split) {
         e = launch_combine(p.ws_o, p.ws_lse, a.o, a.lse, a.batch, a.heads, mq, a.head_dim_v, splits,
@@ -690,6 +704,11 @@ void fa_debug_set(uint64_t wait_limit_ns, uint32_t inject) {
     std::lock_guard<std::mutex> lk(g_mu);
     g_wait_limit_ns = wait_limit_ns ? wait_limit_ns : kDefaultWaitNs;
     g_inject = inject;
+}
+
+void fa_debug_select_steady(int mode) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_steady_mode = (mode == 1 || mode == -1) ? mode : 0;
 }
 
 fa_status fa_debug_trace(void* buf, size_t bytes) {

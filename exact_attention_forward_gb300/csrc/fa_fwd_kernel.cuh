@@ -438,7 +438,13 @@ enum : uint32_t {
 // launch-bound B=1 H=2 S=256 call -15 to -24 %, the 8K shapes within +-0.6 %.  (Folding key
 // splits and packed rows as well made the code smaller still but the 8K launches 1.4-4 %
 // slower.)
-template <int D, bool FP8, bool PAIR = false, bool CACHE = false, bool VAR = true>
+// STEADY: the instance for long fixed-length bf16 launches, whose MMA issuer runs key
+// blocks in the middle of an item (both tiles active, past their first PV) without the
+// per-block tests of the edge blocks.  The single issuing thread paces the tensor pipe, so
+// those tests cost time: same-run A/B, bit-identical outputs, causal and grouped-query 8K
+// -4 %, non-causal 8K -4.7 %.  Its extra code (~10 KB, fetched from DRAM after every L2
+// flush) made short launches 1-3 % slower, so the host picks it by size.
+template <int D, bool FP8, bool PAIR = false, bool CACHE = false, bool VAR = true, bool STEADY = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -987,61 +993,135 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     release_slot(kslot0);
                 }
-                for (int j = j0; j >= lo; --j) {
-                    const uint32_t vslot = ring % C::kStages;
-#ifdef FA_TRACE  // had the group landed when the issuer got here?
-                    tr.ev(mbar_test_wait(bar(C::KV_FULL + vslot), (ph_kv >> vslot) & 1u) ? 11 : 12);
-#endif
-                    if (!wait_kv(vslot)) {  // group {V(j), K(j-1)} (or {V(lo)})
-                        aborted = true;
-                        break;
-                    }
-                    tr.ev(3);
-                    ++ring;
-                    // a tile that does not visit block j releases V(j) at once (its load has
-                    // landed, so the arrival belongs to this phase of the slot)
-                    if (j >= hi0) release_slot(vslot);
-                    if (j >= hi1) release_slot(vslot);
-                    const bool has_next = j - 1 >= lo;
-                    const uint32_t nslot = ring % C::kStages;  // K(j-1), landed with V(j)
-                    if (has_next) ++ring;
-                    // one tile: PV_t(j) if it visits block j, then S_t(j-1) if it visits j-1
-                    auto tile_step = [&](auto tc, int hi, uint32_t& acc) -> bool {
-                        constexpr int t = decltype(tc)::value;
-                        const bool cur = j < hi;
-                        const bool nxt = has_next && (j - 1) < hi;
-                        if (cur) {
-#ifdef FA_TRACE  // was P ready when the issuer got here?
-                            tr.ev(mbar_test_wait(bar(C::P_FULL + t), (ph_p >> t) & 1u) ? 13 : 14);
-#endif
-                            if (!wait_handoff(bar(C::P_FULL + t), (ph_p >> t) & 1u, SITE_P_FULL)) return false;
-                            tr.ev(4 + t);
-                            ph_p ^= 1u << t;
-                            if (acc == 0u &&
-                                !wait_handoff(bar(C::O_EMPTY + t), ((ph_o >> t) & 1u) ^ 1u, SITE_O_EMPTY))
-                                return false;
-                            tc_fence_after();
-                            issue_pv(tc, vslot, acc);
-                            acc = 1u;
+                if constexpr (STEADY) {
+                    // STEADY instance: the body of one key block as a template on kSteady -- both
+                    // tiles visit blocks j and j - 1 and are past their first PV, and no slot is
+                    // released for a skipping tile.  The issuer's instruction stream paces the
+                    // tensor pipe, and in steady blocks it then carries no per-block tests.
+                    auto run_block = [&](const int j, auto steady_c) -> bool {
+                        constexpr bool kSteady = decltype(steady_c)::value;
+                        const uint32_t vslot = ring % C::kStages;
+    #ifdef FA_TRACE  // had the group landed when the issuer got here?
+                        tr.ev(mbar_test_wait(bar(C::KV_FULL + vslot), (ph_kv >> vslot) & 1u) ? 11 : 12);
+    #endif
+                        if (!wait_kv(vslot)) return false;  // group {V(j), K(j-1)} (or {V(lo)})
+                        tr.ev(3);
+                        ++ring;
+                        // a tile that does not visit block j releases V(j) at once (its load has
+                        // landed, so the arrival belongs to this phase of the slot)
+                        if (!kSteady) {
+                            if (j >= hi0) release_slot(vslot);
+                            if (j >= hi1) release_slot(vslot);
                         }
-                        if (nxt) {
-                            issue_qk(tc, nslot);
-                            commit(bar(C::S_FULL + t));
-                            if (FP8 && j - 1 == lo) commit(bar(C::Q_EMPTY + t));
-                        } else if (cur) {
-                            commit(bar(C::O_FULL + t));  // last block of tile t
+                        const bool has_next = kSteady || j - 1 >= lo;
+                        const uint32_t nslot = ring % C::kStages;  // K(j-1), landed with V(j)
+                        if (has_next) ++ring;
+                        // one tile: PV_t(j) if it visits block j, then S_t(j-1) if it visits j-1
+                        auto tile_step = [&](auto tc, int hi, uint32_t& acc) -> bool {
+                            constexpr int t = decltype(tc)::value;
+                            const bool cur = kSteady || j < hi;
+                            const bool nxt = kSteady || (has_next && (j - 1) < hi);
+                            if (cur) {
+    #ifdef FA_TRACE  // was P ready when the issuer got here?
+                                tr.ev(mbar_test_wait(bar(C::P_FULL + t), (ph_p >> t) & 1u) ? 13 : 14);
+    #endif
+                                if (!wait_handoff(bar(C::P_FULL + t), (ph_p >> t) & 1u, SITE_P_FULL)) return false;
+                                tr.ev(4 + t);
+                                ph_p ^= 1u << t;
+                                if (!kSteady && acc == 0u &&
+                                    !wait_handoff(bar(C::O_EMPTY + t), ((ph_o >> t) & 1u) ^ 1u, SITE_O_EMPTY))
+                                    return false;
+                                tc_fence_after();
+                                issue_pv(tc, vslot, kSteady ? 1u : acc);
+                                acc = 1u;
+                            }
+                            if (nxt) {
+                                issue_qk(tc, nslot);
+                                commit(bar(C::S_FULL + t));
+                                if (FP8 && j - 1 == lo) commit(bar(C::Q_EMPTY + t));
+                            } else if (cur) {
+                                commit(bar(C::O_FULL + t));  // last block of tile t
+                            }
+                            tr.ev(6 + t);
+                            return true;
+                        };
+                        if (!tile_step(std::integral_constant<int, 0>{}, hi0, acc0) ||
+                            !tile_step(std::integral_constant<int, 1>{}, hi1, acc1))
+                            return false;
+                        if (!kSteady && has_next) {  // K(j-1) has landed (some tile read it); skipping tiles release it
+                            if (j - 1 >= hi0) release_slot(nslot);
+                            if (j - 1 >= hi1) release_slot(nslot);
                         }
-                        tr.ev(6 + t);
                         return true;
                     };
-                    if (!tile_step(std::integral_constant<int, 0>{}, hi0, acc0) ||
-                        !tile_step(std::integral_constant<int, 1>{}, hi1, acc1)) {
-                        aborted = true;
-                        break;
+                    // steady blocks: lo < j <= min(hi0, hi1) - 2 (both tiles had their first PV at
+                    // block hi_t - 1 > j)
+                    const int j_steady = min(hi0, hi1) - 2;
+                    for (int j = j0; j >= lo; --j) {
+                        const bool ok = (j <= j_steady && j > lo) ? run_block(j, std::true_type{})
+                                                                  : run_block(j, std::false_type{});
+                        if (!ok) {
+                            aborted = true;
+                            break;
+                        }
                     }
-                    if (has_next) {  // K(j-1) has landed (some tile read it); skipping tiles release it
-                        if (j - 1 >= hi0) release_slot(nslot);
-                        if (j - 1 >= hi1) release_slot(nslot);
+                } else {
+                    for (int j = j0; j >= lo; --j) {
+                        const uint32_t vslot = ring % C::kStages;
+    #ifdef FA_TRACE  // had the group landed when the issuer got here?
+                        tr.ev(mbar_test_wait(bar(C::KV_FULL + vslot), (ph_kv >> vslot) & 1u) ? 11 : 12);
+    #endif
+                        if (!wait_kv(vslot)) {  // group {V(j), K(j-1)} (or {V(lo)})
+                            aborted = true;
+                            break;
+                        }
+                        tr.ev(3);
+                        ++ring;
+                        // a tile that does not visit block j releases V(j) at once (its load has
+                        // landed, so the arrival belongs to this phase of the slot)
+                        if (j >= hi0) release_slot(vslot);
+                        if (j >= hi1) release_slot(vslot);
+                        const bool has_next = j - 1 >= lo;
+                        const uint32_t nslot = ring % C::kStages;  // K(j-1), landed with V(j)
+                        if (has_next) ++ring;
+                        // one tile: PV_t(j) if it visits block j, then S_t(j-1) if it visits j-1
+                        auto tile_step = [&](auto tc, int hi, uint32_t& acc) -> bool {
+                            constexpr int t = decltype(tc)::value;
+                            const bool cur = j < hi;
+                            const bool nxt = has_next && (j - 1) < hi;
+                            if (cur) {
+    #ifdef FA_TRACE  // was P ready when the issuer got here?
+                                tr.ev(mbar_test_wait(bar(C::P_FULL + t), (ph_p >> t) & 1u) ? 13 : 14);
+    #endif
+                                if (!wait_handoff(bar(C::P_FULL + t), (ph_p >> t) & 1u, SITE_P_FULL)) return false;
+                                tr.ev(4 + t);
+                                ph_p ^= 1u << t;
+                                if (acc == 0u &&
+                                    !wait_handoff(bar(C::O_EMPTY + t), ((ph_o >> t) & 1u) ^ 1u, SITE_O_EMPTY))
+                                    return false;
+                                tc_fence_after();
+                                issue_pv(tc, vslot, acc);
+                                acc = 1u;
+                            }
+                            if (nxt) {
+                                issue_qk(tc, nslot);
+                                commit(bar(C::S_FULL + t));
+                                if (FP8 && j - 1 == lo) commit(bar(C::Q_EMPTY + t));
+                            } else if (cur) {
+                                commit(bar(C::O_FULL + t));  // last block of tile t
+                            }
+                            tr.ev(6 + t);
+                            return true;
+                        };
+                        if (!tile_step(std::integral_constant<int, 0>{}, hi0, acc0) ||
+                            !tile_step(std::integral_constant<int, 1>{}, hi1, acc1)) {
+                            aborted = true;
+                            break;
+                        }
+                        if (has_next) {  // K(j-1) has landed (some tile read it); skipping tiles release it
+                            if (j - 1 >= hi0) release_slot(nslot);
+                            if (j - 1 >= hi1) release_slot(nslot);
+                        }
                     }
                 }
                 if (aborted) break;
@@ -1509,7 +1589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool FP8, bool PAIR = false, bool CACHE = false, bool VAR = true>
+template <int D, bool FP8, bool PAIR = false, bool CACHE = false, bool VAR = true, bool STEADY = false>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t stream,
                        bool after_append) {
@@ -1523,13 +1603,13 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
     if (e != cudaSuccess) return e;
     const unsigned long long ctx = current_context_id();
     if (dev < 0 || dev >= 64 || ctx == 0 || attr_ctx[dev].load(std::memory_order_acquire) != ctx) {
-        e = cudaFuncSetAttribute(fa_fwd_kernel<D, FP8, PAIR, CACHE, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(fa_fwd_kernel<D, FP8, PAIR, CACHE, VAR, STEADY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_ctx[dev].store(ctx, std::memory_order_release);
     }
     if (!after_append && !PAIR) {
-        fa_fwd_kernel<D, FP8, PAIR, CACHE, VAR><<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, o, p);
+        fa_fwd_kernel<D, FP8, PAIR, CACHE, VAR, STEADY><<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, o, p);
         return cudaGetLastError();
     }
     // after the cache append: programmatic dependent launch, so this grid's set-up
@@ -1557,7 +1637,7 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, FP8, PAIR, CACHE, VAR>, q, k, v, o, p);
+    return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, FP8, PAIR, CACHE, VAR, STEADY>, q, k, v, o, p);
 }
 
 // How many CTA pairs of the kernel can be resident at once (0 if none).
