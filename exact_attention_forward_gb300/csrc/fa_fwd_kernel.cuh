@@ -442,8 +442,9 @@ enum : uint32_t {
 // blocks in the middle of an item (both tiles active, past their first PV) without the
 // per-block tests of the edge blocks.  The single issuing thread paces the tensor pipe, so
 // those tests cost time: same-run A/B, bit-identical outputs, causal and grouped-query 8K
-// -4 %, non-causal 8K -4.7 %.  Its extra code (~10 KB, fetched from DRAM after every L2
-// flush) made short launches 1-3 % slower, so the host picks it by size.
+// -4 %, non-causal 8K -4.7 %, and -1.4 to -1.9 % more once its MMA descriptors stopped
+// spilling.  Its extra code (~9 KB, fetched from DRAM after every L2 flush) made short
+// launches 1-3 % slower, so the host picks it by size.
 template <int D, bool FP8, bool PAIR = false, bool CACHE = false, bool VAR = true, bool STEADY = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -915,7 +916,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // S_t = Q_t K^T : A = Q (K-major), B = K (K-major), both 128B-swizzled.
             auto issue_qk = [&](auto tc, uint32_t kslot) {
                 constexpr int t = decltype(tc)::value;
-                const uint32_t a0 = q_lo + t * kTile16, b0 = k_lo + kslot * kSlot16;
+                uint32_t a0 = q_lo + t * kTile16, b0 = k_lo + kslot * kSlot16;
+                // STEADY: bases taken per call, so the compiler keeps no per-item set of 64-bit
+                // descriptors live across blocks (it spilled them: 60 bytes; without, -1.4 %)
+                if constexpr (STEADY) asm volatile("" : "+r"(a0), "+r"(b0));
 #pragma unroll
                 for (int kk = 0; kk < D / C::kUmmaK; ++kk) {
                     // k step kk: 32 bytes further along the row, next 128-byte atom column
@@ -938,7 +942,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc_pv = (FP8 && p.v_e5m2) ? C::kIdescPV5 : C::kIdescPV;
             auto issue_pv = [&](auto tc, uint32_t vslot, uint32_t acc) {
                 constexpr int t = decltype(tc)::value;
-                const uint32_t b0 = v_lo + vslot * kSlot16;
+                uint32_t b0 = v_lo + vslot * kSlot16;
+                if constexpr (STEADY) asm volatile("" : "+r"(b0));
 #pragma unroll
                 for (int kk = 0; kk < kBN / C::kUmmaK; ++kk) {
                     const uint32_t off = (uint32_t)(kk * C::kUmmaK * 128) >> 4;
