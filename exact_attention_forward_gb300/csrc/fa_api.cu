@@ -52,8 +52,10 @@ uint32_t* g_sched_addr[kMaxDevices] = {nullptr};
 // range [kEagerSlots, kSchedSlots) and never share one with an eager launch.
 constexpr int kEagerSlots = 192;
 // (tile, key block) steps per CTA from which a fixed-length bf16 D = 128 launch takes the
-// kernel instance specialised for steady key blocks
-constexpr double kSteadyMinTileBlocksPerCta = 256.0;
+// kernel instance specialised for steady key blocks.  Measured, both instances from one
+// library, L2 flushed: +5.5 % at 54 per CTA (causal 2K), even at 108-121, -2.8 to -4 % at
+// 215-243, -5.8 % at 431.
+constexpr double kSteadyMinTileBlocksPerCta = 128.0;
 std::atomic<uint32_t> g_sched_next{0};
 std::atomic<uint32_t> g_sched_next_captured{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -651,7 +653,7 @@ fa_status fwd_impl(const FwdArgs& a) {
     // Long fixed-length bf16 D = 128 launches take the instance whose issuer runs the middle
     // key blocks of an item without per-block tests.  Its extra code is fetched from DRAM on
     // every launch after an L2 flush, so it pays off only over enough (tile, key block)
-    // steps per CTA: measured faster at causal 8K (~860 per CTA), slower at causal 2K (~54).
+    // steps per CTA (kSteadyMinTileBlocksPerCta).
     const double tile_blocks = (double)a.batch * p.item_heads * (double)ceil_div((long long)mq * pack, 128) *
                                (double)nblk * (a.causal ? 0.5 : 1.0);
     const bool steady = !fp8 && a.head_dim == 128 && !var && !cache && steady_mode >= 0 &&
