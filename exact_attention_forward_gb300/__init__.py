@@ -170,7 +170,7 @@ def debug_set(wait_limit_ns: int = 0, inject: int = 0) -> None:
 
 
 def debug_select_steady(mode: int = 0) -> None:
-    """Kernel instance of fixed-length bf16 head_dim-128 launches: 0 by size (default),
+    """Kernel instance of bf16 head_dim-128 launches without a cache: 0 by size (default),
     1 always the steady-block instance, -1 never (fa_debug_select_steady)."""
     load_library().fa_debug_select_steady(int(mode))
 

@@ -51,7 +51,7 @@ uint32_t* g_sched_addr[kMaxDevices] = {nullptr};
 // a CUDA graph keep their slot for every replay, so they take theirs from the separate
 // range [kEagerSlots, kSchedSlots) and never share one with an eager launch.
 constexpr int kEagerSlots = 192;
-// (tile, key block) steps per CTA from which a fixed-length bf16 D = 128 launch takes the
+// (tile, key block) steps per CTA from which a bf16 D = 128 launch without a cache takes the
 // kernel instance specialised for steady key blocks.  Measured, both instances from one
 // library, L2 flushed: +5.5 % at 54 per CTA (causal 2K), even at 108-121, -2.8 to -4 % at
 // 215-243, -5.8 % at 431.
@@ -650,13 +650,14 @@ fa_status fwd_impl(const FwdArgs& a) {
     const bool cache = a.seqused_k != nullptr;  // the kernel instance with the cache code
     // the instance with packed variable-length batches (and debug injection)
     const bool var = p.varlen || p.inject != 0u;
-    // Long fixed-length bf16 D = 128 launches take the instance whose issuer runs the middle
+    // Long bf16 D = 128 launches (fixed length or varlen) take the instance whose issuer runs the middle
     // key blocks of an item without per-block tests.  Its extra code is fetched from DRAM on
     // every launch after an L2 flush, so it pays off only over enough (tile, key block)
     // steps per CTA (kSteadyMinTileBlocksPerCta).
+    // (varlen: from the longest sequence's lengths, an upper bound)
     const double tile_blocks = (double)a.batch * p.item_heads * (double)ceil_div((long long)mq * pack, 128) *
                                (double)nblk * (a.causal ? 0.5 : 1.0);
-    const bool steady = !fp8 && a.head_dim == 128 && !var && !cache && steady_mode >= 0 &&
+    const bool steady = !fp8 && a.head_dim == 128 && p.inject == 0u && !cache && steady_mode >= 0 &&
                         (steady_mode == 1 || tile_blocks >= kSteadyMinTileBlocksPerCta * (double)grid);
     if (fp8)
         e = launch_fwd_e4m3_d128(tq, tk, tv, to, p, grid, s, append && !fused_append, cache, var);

@@ -438,7 +438,7 @@ enum : uint32_t {
 // launch-bound B=1 H=2 S=256 call -15 to -24 %, the 8K shapes within +-0.6 %.  (Folding key
 // splits and packed rows as well made the code smaller still but the 8K launches 1.4-4 %
 // slower.)
-// STEADY: the instance for long fixed-length bf16 launches, whose MMA issuer runs key
+// STEADY: the instance for long bf16 launches (fixed length or varlen), whose MMA issuer runs key
 // blocks in the middle of an item (both tiles active, past their first PV) without the
 // per-block tests of the edge blocks.  The single issuing thread paces the tensor pipe, so
 // those tests cost time: same-run A/B, bit-identical outputs, causal and grouped-query 8K

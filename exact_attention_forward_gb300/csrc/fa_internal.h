@@ -84,7 +84,7 @@ constexpr size_t kTraceBytes = (size_t)kTraceCtas * kTraceRoles * kTraceCap * si
 cudaError_t launch_fwd_bf16_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                 const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t s,
                                 bool after_append, bool cache, bool var);
-// steady (bf16 D = 128 only): the fixed-length instance specialised for long launches
+// steady (bf16 D = 128 only): the instance specialised for long launches (fixed length or varlen)
 cudaError_t launch_fwd_bf16_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                  const CUtensorMap& o, const FwdParams& p, int grid, cudaStream_t s,
                                 bool after_append, bool cache, bool var, bool steady);

@@ -325,12 +325,12 @@ FA_API fa_status fa_device_error(uint32_t* flags, int clear);
 FA_API void fa_debug_set(uint64_t wait_limit_ns, uint32_t inject);
 
 /*
- * Debug: which kernel instance fixed-length bf16 head_dim-128 launches without a
- * key/value cache use (process-wide, host side, applied to subsequent launches).
- * Those launches have two instances with identical results: one for short launches
- * and one whose MMA issuer runs the middle key blocks of a work item without
- * per-block tests, which the library picks once a launch holds at least 128
- * (query tile, key block) steps per CTA.  mode: 0 = by that size (the default),
+ * Debug: which kernel instance bf16 head_dim-128 launches without a key/value cache
+ * use (process-wide, host side, applied to subsequent launches).  Those launches
+ * (fixed-length or packed varlen) have two instances with identical results: one for
+ * short launches and one whose MMA issuer runs the middle key blocks of a work item
+ * without per-block tests, which the library picks once a launch holds at least 128
+ * (query tile, key block) steps per CTA (varlen: counted from the longest sequence).  mode: 0 = by that size (the default),
  * 1 = always the steady-block instance, -1 = never.  Other values: as 0.  For
  * tests that exercise both instances on small shapes.
  */

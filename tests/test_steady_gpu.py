@@ -1,8 +1,8 @@
-"""GPU: the kernel instance for long fixed-length bf16 launches (the MMA issuer runs the
-middle key blocks of a work item without per-block tests).  The library picks it by
-launch size; here fa_debug_select_steady forces it onto small shapes -- ragged query
-and key tails, causal with Sq < Sk and Sq > Sk, items of one and two key blocks,
-grouped K/V heads -- compared element by element with the fp64 oracle (outputs
+"""GPU: the kernel instances for long bf16 head_dim-128 launches (the MMA issuer runs the
+middle key blocks of a work item without per-block tests), fixed-length and packed
+varlen.  The library picks them by launch size; here fa_debug_select_steady forces them
+onto small shapes -- ragged query and key tails, causal with Sq < Sk and Sq > Sk, items of
+one and two key blocks, grouped K/V heads, packed sequences with empty ranges -- compared element by element with the fp64 oracle (outputs
 pre-filled with NaN) and byte for byte with the other instance, which issues the same
 MMAs in the same order."""
 import numpy as np
@@ -75,4 +75,18 @@ def test_steady_instance_causal_2k_workload_bit_identical():
     w = inputs.WORKLOADS["bf16_causal_2k"]
     x = workload_inputs("bf16_causal_2k")
     (o1, l1), (o0, l0) = _both(x, causal=w.causal, softmax_scale=w.softmax_scale)
+    assert np.array_equal(o1, o0) and np.array_equal(l1, l0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_steady_instance_varlen(causal):
+    # packed sequences: empty query or key ranges, one-block and many-block items
+    sq = [5, 0, 130, 1300, 1, 128, 900]
+    sk = [7, 3, 0, 1500, 1, 128, 2000]
+    x = inputs.make_varlen(sq, sk, heads=3, head_dim=128, seed=29)
+    scale = 128 ** -0.5
+    (o1, l1), (o0, l0) = _both(x, causal=causal, softmax_scale=scale)
+    o_ref, lse_ref = oracle.attention(x["q"], x["k"], x["v"], softmax_scale=scale, causal=causal,
+                                      cu_seqlens_q=x["cu_seqlens_q"], cu_seqlens_k=x["cu_seqlens_k"])
+    compare(o1, l1, o_ref, lse_ref, what=f"steady instance, varlen causal={causal}")
     assert np.array_equal(o1, o0) and np.array_equal(l1, l0)
