@@ -1071,6 +1071,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 } else {
+                    // the other instances keep the block loop as it stood before the steady
+                    // instance: routing them through run_block changes their code, and every
+                    // change to the issuer's code moved their launches by 1-3 %
                     for (int j = j0; j >= lo; --j) {
                         const uint32_t vslot = ring % C::kStages;
     #ifdef FA_TRACE  // had the group landed when the issuer got here?
